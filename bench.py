@@ -1,0 +1,529 @@
+"""Benchmark of the CSA2 FP4-KV decode hot path on one B300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl csa2|reference]
+
+A step is one decode step of the configured CSA2 layer group(s) over a batch
+of sequences whose caches are resident in HBM: append the new token (FP4
+quantise of its main-KV row, indexer-key append + block mean, each layer's
+SWA ring), then every group (Full or Reindex indexer, Top-512, sparse
+attention of the first layer and of each Reuse layer). The default workload
+(--config 2) is the decoder layer group Full + 3 Reuse at batch 32 and
+131,072 positions, 64 heads, indexer 8 x 128. The metric is decode tokens/s
+per layer group (one new token per sequence per step), with the Full
+indexer scan's achieved HBM bandwidth as the roofline figure.
+
+Inputs are seeded and synthetic (synth/). With --impl reference the CPU
+oracle is timed instead, on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (sequences are independent; no data-path
+collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode tokens/s per layer group at 128K/1M ctx; % of B300 HBM roofline"
+UNIT = "tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6400.0
+SCAN_BYTES_PER_POS = lambda d_I: d_I + 4       # indexer key read + fp32 score written
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the workload
+# ---------------------------------------------------------------------------
+class DecodeWorkload:
+    """Caches, per-layer inputs and the per-step calls of one decode config."""
+
+    def __init__(self, cfg, device, seed=1234, batch=None):
+        import torch
+        import synth
+        from fp4_kv_cache_06_b300 import csa2
+        self.torch, self.csa2 = torch, csa2
+        self.cfg = cfg
+        self.dev = device
+        B = self.B = batch or cfg.B
+        d_I, H_I, H, W, k, P = cfg.d_I, cfg.H_I, cfg.H, cfg.W, cfg.k, cfg.P
+        self.n_end = cfg.n                               # positions visible after the last step
+        self.n_first = cfg.n_start + 1 if cfg.steps > 1 else cfg.n
+        self.n_cap = cfg.n
+        n_pre = self.n_first - 1                         # positions cached before the first step
+        self.layers = sum(1 + g[1] for g in cfg.groups)
+        dev = device
+        u8, i64, i32 = torch.uint8, torch.int64, torch.int32
+        self.codes = torch.empty((B, self.n_cap, 256), dtype=u8, device=dev)
+        self.scales = torch.empty((B, self.n_cap, 32), dtype=u8, device=dev)
+        self.kI = torch.empty((B, self.n_cap, d_I), dtype=u8, device=dev)
+        self.kbar = torch.zeros((B, (self.n_cap + 7) // 8, d_I), dtype=u8, device=dev)
+        chunk = 1 << 17
+        for b in range(B):                               # main KV: bf16 N(0,1) -> FP4 (resident)
+            for c0 in range(0, n_pre, chunk):
+                r = min(chunk, n_pre - c0)
+                x = synth.normal_bf16((1, r, 512), seed, "kv", dev, sub=b * 4096 + c0 // chunk)
+                csa2.csa2_quantize_kv_fp4(x, self.codes[b:b + 1], self.scales[b:b + 1],
+                                          pos=torch.tensor([c0], dtype=i64, device=dev))
+            self.kI[b, :n_pre] = synth.indexer_keys_e4m3((n_pre, d_I), seed, dev, bias_prob=cfg.bias_prob, sub=b)
+        nt = torch.full((B,), n_pre, dtype=i64, device=dev)
+        if n_pre > 0:
+            csa2.csa2_block_means(self.kI, nt, self.kbar, n_max=n_pre)
+        self.swa = [synth.normal_bf16((B, W, 512), seed, "swa", dev, sub=l) for l in range(self.layers)]
+        self.q = [synth.normal_bf16((B, H, 512), seed, "q", dev, sub=l) for l in range(self.layers)]
+        self.out = [torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev) for _ in range(self.layers)]
+        G = len(cfg.groups)
+        self.qI = [synth.normal_e4m3((B, H_I, d_I), seed, "qI", dev, sub=g) for g in range(G)]
+        self.w = [synth.uniform_f32((B, H_I), seed, "w", dev, sub=g) for g in range(G)]
+        self.qI_pool = synth.normal_e4m3((B, H_I, d_I), seed, "qI_pool", dev)
+        self.w_pool = synth.uniform_f32((B, H_I), seed, "w_pool", dev)
+        self.kv_new = synth.normal_bf16((B, 1, 512), seed, "kv_new", dev)
+        self.kI_new = synth.indexer_keys_e4m3((B, 1, d_I), seed + 1, dev, bias_prob=cfg.bias_prob)
+        self.swa_new = [synth.normal_bf16((B, 512), seed, "swa_new", dev, sub=l) for l in range(self.layers)]
+        self.idx = [torch.empty((B, k), dtype=i32, device=dev) for _ in range(G)]
+        self.pool = torch.full((B, P), -1, dtype=i32, device=dev)
+        self.pos = torch.full((B,), n_pre, dtype=i64, device=dev)
+        self.n = torch.full((B,), n_pre + 1, dtype=i64, device=dev)
+        self.swa_len = torch.full((B,), min(n_pre + 1, W), dtype=i32, device=dev)
+        self.ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_LAYER_GROUP, B, self.n_cap, k, P, H), dev)
+        self.step_i = 0
+        torch.cuda.synchronize()
+
+    def reset_positions(self):
+        """Restart the step sequence (positions back to the first step's)."""
+        self.step_i = 0
+        self.pos.fill_(self.n_first - 1)
+        self.n.fill_(self.n_first)
+
+    def step(self, events=None):
+        """One decode step; `events` (optional) = per-group lists of CUDA events."""
+        csa2, cfg = self.csa2, self.cfg
+        if self.step_i > 0 and self.cfg.steps > 1:
+            self.pos.add_(1)
+            self.n.add_(1)
+        csa2.csa2_quantize_kv_fp4(self.kv_new, self.codes, self.scales, pos=self.pos)
+        csa2.csa2_append_indexer_k(self.kI_new, self.kI, self.kbar, pos=self.pos)
+        for l in range(self.layers):
+            csa2.csa2_append_swa(self.swa_new[l], self.pos, self.swa[l])
+        n_max = self.n_first + (self.cfg.steps - 1 if self.cfg.steps > 1 else 0)
+        n_max = min(n_max, self.n_cap)
+        l0 = 0
+        for g, (mode, n_reuse, form_pool) in enumerate(cfg.groups):
+            L = 1 + n_reuse
+            csa2.csa2_layer_group(
+                csa2.MODE_FULL if mode == "full" else csa2.MODE_REINDEX, self.n, n_max, self.codes, self.scales,
+                self.kI, self.qI[g], self.w[g], self.idx[g], self.q[l0:l0 + L], self.swa[l0:l0 + L], self.swa_len,
+                self.out[l0:l0 + L], self.ws, kbar=self.kbar, pool=self.pool, form_pool=form_pool,
+                qI_pool=self.qI_pool if mode == "reindex" else None,
+                w_pool=self.w_pool if mode == "reindex" else None,
+                events=None if events is None else events[g])
+            l0 += L
+        self.step_i += 1
+
+    def scan_positions(self):
+        """Positions the Full scans of one step read (for the roofline)."""
+        return sum(self.B * min(self.n_end, self.n_cap) for (m, _, _) in self.cfg.groups if m == "full")
+
+    # host-side step for the end-to-end figure: per-step inputs from pinned host memory
+    def host_buffers(self):
+        torch = self.torch
+        self.h_in = {
+            "kv_new": self.kv_new.cpu().pin_memory(), "kI_new": self.kI_new.cpu().pin_memory(),
+            "swa_new": [t.cpu().pin_memory() for t in self.swa_new], "q": [t.cpu().pin_memory() for t in self.q],
+            "qI": [t.cpu().pin_memory() for t in self.qI], "w": [t.cpu().pin_memory() for t in self.w],
+        }
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.out]
+        hi = self.h_in
+        h2d = hi["kv_new"].numel() * 2 + hi["kI_new"].numel() + sum(t.numel() * 2 for t in hi["swa_new"]) + \
+            sum(t.numel() * 2 for t in hi["q"]) + sum(t.numel() for t in hi["qI"]) + sum(t.numel() * 4 for t in hi["w"])
+        d2h = sum(t.numel() * 2 for t in self.h_out)
+        return h2d, d2h
+
+    def step_e2e(self):
+        hi = self.h_in
+        self.kv_new.copy_(hi["kv_new"], non_blocking=True)
+        self.kI_new.copy_(hi["kI_new"], non_blocking=True)
+        for d, s in zip(self.swa_new, hi["swa_new"]):
+            d.copy_(s, non_blocking=True)
+        for d, s in zip(self.q, hi["q"]):
+            d.copy_(s, non_blocking=True)
+        for d, s in zip(self.qI, hi["qI"]):
+            d.copy_(s, non_blocking=True)
+        for d, s in zip(self.w, hi["w"]):
+            d.copy_(s, non_blocking=True)
+        self.step()
+        for d, s in zip(self.h_out, self.out):
+            d.copy_(s, non_blocking=True)
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def scan_traffic(d_I, positions_per_launch):
+    """DRAM bytes per Full-scan launch from the committed ncu summary, if the
+    scan kernel's source is unchanged since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "index_scan_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, "fp4_kv_cache_06_b300", "csrc", "index_scan.cu")
+        if rec.get("source_sha256_16") != source_hash(src):
+            return None
+        return rec["dram_bytes_per_position"] * positions_per_launch
+    except Exception:
+        return None
+
+
+def run_csa2(args, world, rank, local):
+    import torch
+    import synth
+    from fp4_kv_cache_06_b300 import csa2
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.get_config(args.config)
+    if cfg.prefill_queries:
+        raise SystemExit("the prefill configuration is not a decode bench workload")
+    wl = DecodeWorkload(cfg, dev, seed=1234 + 7919 * rank, batch=args.batch)
+    G = len(cfg.groups)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    total_steps = args.warmup + args.steps
+    if cfg.steps > 1 and total_steps > cfg.steps:
+        pass  # positions wrap below so the cache never exceeds its capacity
+
+    def maybe_wrap():
+        if cfg.steps > 1 and wl.step_i >= cfg.steps:
+            wl.reset_positions()
+
+    for _ in range(args.warmup):
+        maybe_wrap()
+        wl.step()
+    torch.cuda.synchronize()
+    if cfg.steps > 1:
+        wl.reset_positions()
+
+    # per-group events: [0] scan start, [1] scan end, [2] after Top-K/pool, then one per layer
+    def mk():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+    step_ev = [(mk(), mk()) for _ in range(args.steps)]
+    grp_ev = [[[mk() for _ in range(3 + 1 + cfg.groups[g][1])] for g in range(G)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    launches0 = csa2.launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            maybe_wrap()
+            flush.zero_()                                  # evict L2 between steps (outside the step events)
+            step_ev[i][0].record()
+            wl.step(events=grp_ev[i])
+            step_ev[i][1].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    launches = csa2.launch_count() - launches0
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, dev)
+    # Full scan duration (events 0 -> 1 of each Full group)
+    scan_ms = []
+    for i in range(args.steps):
+        for g, (mode, _, _) in enumerate(cfg.groups):
+            if mode == "full":
+                scan_ms.append(grp_ev[i][g][0].elapsed_time(grp_ev[i][g][1]))
+    phase = {}
+    for g, (mode, nr, fp) in enumerate(cfg.groups):
+        ev = [[grp_ev[i][g][j] for j in range(3 + 1 + nr)] for i in range(args.steps)]
+        phase[f"group{g}_{mode}"] = {
+            "indexer_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
+            "topk_pool_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in ev),
+            "attn_ms_per_layer": statistics.mean(e[2 + j].elapsed_time(e[3 + j]) for e in ev for j in range(1 + nr)),
+        }
+
+    # end-to-end: per-step inputs from pinned host memory, outputs back to host
+    e2e = None
+    if not args.no_e2e:
+        h2d, d2h = wl.host_buffers()
+        if cfg.steps > 1:
+            wl.reset_positions()
+        for _ in range(2):
+            maybe_wrap()
+            wl.step_e2e()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record()
+        for i in range(args.steps):
+            maybe_wrap()
+            wl.step_e2e()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+        e2e = {"value": world * wl.B / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    hbm, hbm_kind = peaks()
+    roof = None
+    if scan_ms:
+        per_launch_pos = wl.B * min(wl.n_end, wl.n_cap)
+        alg = per_launch_pos * SCAN_BYTES_PER_POS(cfg.d_I)
+        scan_avg = statistics.mean(scan_ms)
+        ach = alg / (scan_avg / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "k_index_scan (Full indexer scan)", "achieved": round(ach, 1),
+                "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                "traffic": scan_traffic(cfg.d_I, per_launch_pos), "algorithmic_bytes_per_launch": alg,
+                "scan_ms": round(scan_avg, 4)}
+    res = {
+        "metric": METRIC, "value": world * wl.B / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
+        "config": {"workload": cfg.workload, "config_index": args.config, "batch": wl.B,
+                   "context": wl.n_end, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}", "topk": cfg.k,
+                   "swa": cfg.W, "groups": [list(g) for g in cfg.groups], "parallelism": f"replicas{world}",
+                   "l2": "flushed before every step (256 MiB write outside the per-step events)"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
+        "phases_ms": phase, "wall_s": wall, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+    }
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """One decode step of ONE sequence of the config, run by the oracle.
+
+    Inputs are generated once (untimed); step() is the timed part: the new
+    token's FP4 append, the group's indexer over every position (Full) or
+    block means + pool + Reindex, Top-512, and each layer's attention. The
+    FP4 rows a step reads are quantised by the oracle inside the step from
+    their bf16 source rows (the oracle keeps no FP4 cache of its own)."""
+
+    def __init__(self, cfg, seed=99):
+        import numpy as np
+        import torch
+        import synth
+        self.cfg = cfg
+        n, d_I, H_I, H = cfg.n, cfg.d_I, cfg.H_I, cfg.H
+        self.kI = synth.indexer_keys_e4m3((n, d_I), seed, bias_prob=cfg.bias_prob).numpy()
+        chunk = 1 << 16
+        self.kv = np.empty((n, 512), dtype=np.uint16)
+        for c0 in range(0, n, chunk):
+            r = min(chunk, n - c0)
+            self.kv[c0:c0 + r] = synth.normal_bf16((r, 512), seed, "kv", sub=c0 // chunk).view(torch.int16).numpy().view(np.uint16)
+        self.L = 1 + cfg.groups[0][1]
+        bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+        self.q = [bits(synth.normal_bf16((H, 512), seed, "q", sub=l)) for l in range(self.L)]
+        self.swa = [bits(synth.normal_bf16((cfg.W, 512), seed, "swa", sub=l)) for l in range(self.L)]
+        self.qI = synth.normal_e4m3((H_I, d_I), seed, "qI").numpy()
+        self.w = synth.uniform_f32((H_I,), seed, "w").numpy()
+        self.codes = np.zeros((n, 256), dtype=np.uint8)
+        self.scales = np.zeros((n, 32), dtype=np.uint8)
+        mode = cfg.groups[0][0]
+        self.desc = (f"one sequence (batch 1) of the {cfg.workload} step: FP4 append, "
+                     f"{'Full scan of all ' + str(n) + ' positions' if mode == 'full' else 'block means + pool + Reindex'}, "
+                     f"Top-{cfg.k}, {self.L} attention layers; gathered rows quantised inside the step")
+
+    def step(self):
+        import numpy as np
+        import oracle
+        cfg, n = self.cfg, self.cfg.n
+        t0 = time.perf_counter()
+        oracle.quantize_fp4(self.kv[n - 1:n])
+        if cfg.groups[0][0] == "full":
+            idx, _ = oracle.full_topk(self.qI, self.w, self.kI, n, cfg.k)
+        else:
+            kbar = oracle.block_means(self.kI, n)
+            pool, _ = oracle.form_pool(self.qI, self.w, kbar, cfg.P)
+            idx, _, _ = oracle.reindex_topk(self.qI, self.w, self.kI, pool, n, cfg.k)
+        rows = idx[idx >= 0]
+        self.codes[rows], self.scales[rows] = oracle.quantize_fp4(self.kv[rows])
+        for l in range(self.L):
+            oracle.sparse_attention(self.q[l], self.codes, self.scales, idx, self.swa[l], cfg.W)
+        return time.perf_counter() - t0
+
+
+def oracle_baseline(cfg, min_s=10.0, max_steps=30):
+    """Time the oracle's sample step repeatedly for about min_s seconds."""
+    smp = OracleSample(cfg)
+    times = []
+    while sum(times) < min_s and len(times) < max_steps:
+        times.append(smp.step())
+    t = statistics.mean(times)
+    return t, smp.desc + f"; mean of {len(times)} steps"
+
+
+def oracle_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        return max([int(i.get("num_threads", 1)) for i in threadpool_info()] + [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, world, rank):
+    import synth
+    cfg = synth.get_config(args.config)
+    smp = OracleSample(cfg)
+    for _ in range(args.warmup):
+        smp.step()
+    times = [smp.step() for _ in range(args.steps)]
+    desc = smp.desc + f"; mean of {len(times)} steps"
+    t = statistics.mean(times)
+    value = 1.0 / t
+    cores = oracle_cores()
+    return {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.workload, "config_index": args.config, "batch": 1, "context": cfg.n},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
+    ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "csa2":
+        args.warmup = 3
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(args, world, 0)), flush=True)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    res = run_csa2(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            import synth
+            dt, desc = oracle_baseline(synth.get_config(args.config))
+            res["cpu_baseline"] = {"value": 1.0 / dt, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
+                                   "sample": desc}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

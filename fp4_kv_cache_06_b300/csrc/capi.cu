@@ -1,0 +1,381 @@
+// capi.cu — the extern "C" boundary of libcsa2.so: host-side validation,
+// workspace carving and the CSA2 layer-group orchestration.
+//
+// [CSA2] wire.sakhanda.co, "DeepSeek AI выпустила DeepSeek-V4.1-Flash ...",
+//        section "Сжатое разреженное внимание 2 (CSA2)": static layer modes
+//        Full / Reindex / Reuse; the Full layer forms the hierarchical pool.
+// [TG]   tgviewer.app, "DeepSeek-V4.1-Flash: Frontier Agents on a Smaller
+//        Memory Budget", CSA2 bullet: Reuse layers share the Top-K indices and
+//        skip re-scoring.
+//
+// Every entry point validates its arguments on the host, enqueues its
+// kernels on the caller's stream and returns a csa2_status; nothing here
+// synchronises the host or allocates device memory.
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace csa2 {
+
+// ---- kernels' host launchers (defined in the other translation units) -------
+int launch_quantize_fp4(const void* x, int B, int64_t rows, const int64_t* pos, uint8_t* codes,
+                        uint8_t* scales, int64_t n_cap, int32_t* st, cudaStream_t s);
+int launch_append_indexer_k(const uint8_t* k_new, int B, int64_t rows, int d_I, const int64_t* pos,
+                            uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st, cudaStream_t s);
+int launch_block_means(const uint8_t* kI, int B, int d_I, const int64_t* n, int64_t n_max,
+                       int64_t n_cap, uint8_t* kbar, int32_t* st, cudaStream_t s);
+int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa, int W,
+                      cudaStream_t s);
+int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                      const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
+                      int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
+                      uint32_t* hist, int32_t* st, cudaStream_t s);
+size_t topk_ws_bytes(int B);
+uint32_t* topk_ws_hist(void* ws);
+int topk_prepare(void* ws, int B, cudaStream_t s);
+int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, const int64_t* n,
+                int len_div, int B, int64_t n_max, int k, int32_t* idx_out, void* ws, bool hist_ready,
+                cudaStream_t s);
+int topk_init_attributes();
+int attn_init_attributes();
+int attn_splits(int B, int H, int k, int W);
+size_t attn_ws_bytes(int B, int H, int k, int W);
+int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                       int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
+                       int64_t swa_seq_stride, int W, const int32_t* swa_len, float softmax_scale,
+                       void* out, void* ws, int32_t* st, cudaStream_t s);
+
+// ---- bookkeeping --------------------------------------------------------------
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+int launch_status() { return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+// Kernel attributes (dynamic shared memory above 48 KB) are set once per
+// device, on the first call that runs on it.
+static int ensure_init() {
+  static std::mutex mu;
+  static uint64_t done_mask = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done_mask & (1ull << dev)) return CSA2_OK;
+  int rc = topk_init_attributes();
+  if (rc == CSA2_OK) rc = attn_init_attributes();
+  if (rc == CSA2_OK) done_mask |= (1ull << dev);
+  return rc;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+static bool ws_ok(const void* ws, size_t have, size_t need) {
+  return need == 0 || (ws != nullptr && have >= need && (reinterpret_cast<uintptr_t>(ws) & 255) == 0);
+}
+
+// Workspace needs of the individual ops.
+static size_t ws_index_full(int B, int64_t n_max) {
+  return align256((size_t)B * (size_t)n_max * 4) + topk_ws_bytes(B);
+}
+static size_t ws_reindex(int B, int P) {
+  const size_t slots = (size_t)B * (size_t)P * kBlock;
+  return align256(slots * 4) * 2 + topk_ws_bytes(B);
+}
+static size_t ws_form_pool(int B, int64_t n_max) {
+  const int64_t nb = (n_max + kBlock - 1) / kBlock;
+  return align256((size_t)B * (size_t)nb * 4) + topk_ws_bytes(B);
+}
+
+static bool topk_k_ok(int k) { return k >= 1 && k <= kMaxTopK; }
+
+static int rec(cudaEvent_t e, cudaStream_t s) {
+  if (e == nullptr) return CSA2_OK;
+  return cudaEventRecord(e, s) == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+}
+
+// Full indexer: zero the Top-K header, scan with the fused histogram, select.
+// e_begin / e_end (optional) are recorded around the scan kernel alone.
+static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                        const int64_t* n, int B, int H_I, int d_I, int64_t n_max, int k, int32_t* idx_out,
+                        float* scores_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t e_begin,
+                        cudaEvent_t e_end) {
+  int rc;
+  float* scores = scores_out ? scores_out : static_cast<float*>(ws);
+  void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)n_max * 4);
+  if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
+  if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
+  if ((rc = launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, n_max, nullptr, 0,
+                              nullptr, topk_ws_hist(tk), st, s)) != CSA2_OK)
+    return rc;
+  if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
+  return launch_topk(scores, nullptr, n_max, n, 1, B, n_max, k, idx_out, tk, true, s);
+}
+
+static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, int64_t kbar_seq_stride,
+                        const int64_t* n, int B, int H_I, int d_I, int64_t n_max, int P, int32_t* pool_out,
+                        void* ws, int32_t* st, cudaStream_t s) {
+  int rc;
+  const int64_t nb_max = (n_max + kBlock - 1) / kBlock;     // rows of block means
+  float* scores = static_cast<float*>(ws);
+  void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)nb_max * 4);
+  if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
+  if ((rc = launch_index_scan(qI, w, kbar, kbar_seq_stride, n, kBlock, B, H_I, d_I, nb_max, scores, nb_max,
+                              nullptr, 0, nullptr, topk_ws_hist(tk), st, s)) != CSA2_OK)
+    return rc;
+  return launch_topk(scores, nullptr, nb_max, n, kBlock, B, nb_max, P, pool_out, tk, true, s);
+}
+
+static int reindex_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                           const int64_t* n, const int32_t* pool, int P, int B, int H_I, int d_I, int k,
+                           int32_t* idx_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t e_begin,
+                           cudaEvent_t e_end) {
+  int rc;
+  const int64_t slots = (int64_t)P * kBlock;
+  float* scores = static_cast<float*>(ws);
+  int32_t* cpos = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + align256((size_t)B * slots * 4));
+  void* tk = static_cast<char*>(ws) + 2 * align256((size_t)B * slots * 4);
+  if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
+  if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
+  // The pool scan writes every one of the P*8 slots of every row (absent
+  // positions carry cand_pos -1), so Top-K takes all slots of each row.
+  if (P > 0 && (rc = launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, INT64_MAX, scores, slots,
+                                       pool, P, cpos, topk_ws_hist(tk), st, s)) != CSA2_OK)
+    return rc;
+  if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
+  return launch_topk(scores, cpos, slots, nullptr, 1, B, slots, k, idx_out, tk, true, s);
+}
+static bool index_dims_ok(int H_I, int d_I) { return H_I >= 1 && H_I <= 8 && (d_I == 64 || d_I == 128); }
+
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+const char* csa2_status_string(int status) {
+  switch (status) {
+    case CSA2_OK: return "CSA2_OK";
+    case CSA2_ERR_INVALID_ARG: return "CSA2_ERR_INVALID_ARG";
+    case CSA2_ERR_UNSUPPORTED_SHAPE: return "CSA2_ERR_UNSUPPORTED_SHAPE";
+    case CSA2_ERR_WORKSPACE: return "CSA2_ERR_WORKSPACE";
+    case CSA2_ERR_CUDA: return "CSA2_ERR_CUDA";
+    case CSA2_ERR_TIMEOUT: return "CSA2_ERR_TIMEOUT";
+    case CSA2_ERR_DEVICE_BOUNDS: return "CSA2_ERR_DEVICE_BOUNDS";
+    default: return "CSA2_ERR_UNKNOWN";
+  }
+}
+
+int csa2_version(void) { return 100; }
+
+uint64_t csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k, int32_t P, int32_t H) {
+  if (B < 0 || n_max < 0) return 0;
+  switch (op) {
+    case CSA2_OP_TOPK: return topk_ws_bytes(B);
+    case CSA2_OP_INDEX_FULL: return ws_index_full(B, n_max);
+    case CSA2_OP_INDEX_REINDEX: return ws_reindex(B, P);
+    case CSA2_OP_FORM_POOL: return ws_form_pool(B, n_max);
+    case CSA2_OP_SPARSE_ATTN: return attn_ws_bytes(B, H, k, 128);
+    case CSA2_OP_LAYER_GROUP: {
+      size_t m = ws_index_full(B, n_max);
+      const size_t r = ws_reindex(B, P), f = ws_form_pool(B, n_max), a = attn_ws_bytes(B, H, k, 128);
+      if (r > m) m = r;
+      if (f > m) m = f;
+      if (a > m) m = a;
+      return m;
+    }
+    default: return 0;
+  }
+}
+
+int csa2_quantize_kv_fp4(const void* x, int32_t B, int64_t rows, int32_t d, const int64_t* pos,
+                         uint8_t* codes, uint8_t* scales, int64_t n_cap, int32_t* d_status,
+                         void* stream) {
+  if (B < 0 || rows < 0 || n_cap < 0) return CSA2_ERR_INVALID_ARG;
+  if (d != 512) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)B * rows == 0) return CSA2_OK;
+  if (!x || !codes || !scales || !aligned16(x) || !aligned16(codes) || !aligned16(scales))
+    return CSA2_ERR_INVALID_ARG;
+  return launch_quantize_fp4(x, B, rows, pos, codes, scales, n_cap, d_status,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int csa2_append_indexer_k(const uint8_t* k_new, int32_t B, int64_t rows, int32_t d_I,
+                          const int64_t* pos, uint8_t* kI, uint8_t* kbar, int64_t n_cap,
+                          int32_t* d_status, void* stream) {
+  if (B < 0 || rows < 0 || n_cap < 0) return CSA2_ERR_INVALID_ARG;
+  if (d_I != 64 && d_I != 128) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)B * rows == 0) return CSA2_OK;
+  if (!k_new || !kI || !aligned16(k_new) || !aligned16(kI) || (kbar && !aligned16(kbar)))
+    return CSA2_ERR_INVALID_ARG;
+  return launch_append_indexer_k(k_new, B, rows, d_I, pos, kI, kbar, n_cap, d_status,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+int csa2_block_means(const uint8_t* kI, int32_t B, int32_t d_I, const int64_t* n, int64_t n_max,
+                     int64_t n_cap, uint8_t* kbar, int32_t* d_status, void* stream) {
+  if (B < 0 || n_max < 0 || n_max > n_cap) return CSA2_ERR_INVALID_ARG;
+  if (d_I != 64 && d_I != 128) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0 || n_max == 0) return CSA2_OK;
+  if (!kI || !kbar || !n || !aligned16(kI) || !aligned16(kbar)) return CSA2_ERR_INVALID_ARG;
+  return launch_block_means(kI, B, d_I, n, n_max, n_cap, kbar, d_status,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int csa2_append_swa(const void* x, int32_t B, int32_t d, const int64_t* pos, void* swa, int32_t W,
+                    void* stream) {
+  if (B < 0 || W <= 0) return CSA2_ERR_INVALID_ARG;
+  if (d != 512) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!x || !pos || !swa || !aligned16(x) || !aligned16(swa)) return CSA2_ERR_INVALID_ARG;
+  return launch_append_swa(x, B, d, pos, swa, W, static_cast<cudaStream_t>(stream));
+}
+
+int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                      const int64_t* n, int32_t B, int32_t H_I, int32_t d_I, int64_t n_max,
+                      float* scores, int64_t scores_stride, int32_t* d_status, void* stream) {
+  if (B < 0 || n_max < 0 || kI_seq_stride < 0 || scores_stride < n_max) return CSA2_ERR_INVALID_ARG;
+  if (!index_dims_ok(H_I, d_I)) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0 || n_max == 0) return CSA2_OK;
+  if (!qI || !w || !kI || !n || !scores || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
+  return launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, scores_stride,
+                           nullptr, 0, nullptr, nullptr, d_status, static_cast<cudaStream_t>(stream));
+}
+
+int csa2_topk(const float* scores, const int32_t* cand_pos, int64_t scores_stride, const int64_t* n,
+              int32_t B, int64_t n_max, int32_t k, int32_t* idx_out, void* ws, size_t ws_bytes,
+              void* stream) {
+  if (B < 0 || n_max < 0 || scores_stride < n_max) return CSA2_ERR_INVALID_ARG;
+  if (!topk_k_ok(k) || n_max > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!scores || !idx_out) return CSA2_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, topk_ws_bytes(B))) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return launch_topk(scores, cand_pos, scores_stride, n, 1, B, n_max, k, idx_out, ws, false,
+                     static_cast<cudaStream_t>(stream));
+}
+
+int csa2_index_full(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                    const int64_t* n, int32_t B, int32_t H_I, int32_t d_I, int64_t n_max, int32_t k,
+                    int32_t* idx_out, float* scores_out, void* ws, size_t ws_bytes,
+                    int32_t* d_status, void* stream) {
+  if (B < 0 || n_max < 0 || kI_seq_stride < 0) return CSA2_ERR_INVALID_ARG;
+  if (!index_dims_ok(H_I, d_I) || !topk_k_ok(k) || n_max > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!qI || !w || !kI || !n || !idx_out || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, ws_index_full(B, n_max))) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return full_indexer(qI, w, kI, kI_seq_stride, n, B, H_I, d_I, n_max, k, idx_out, scores_out, ws, d_status,
+                      static_cast<cudaStream_t>(stream), nullptr, nullptr);
+}
+
+int csa2_form_pool(const uint8_t* qI, const float* w, const uint8_t* kbar, int64_t kbar_seq_stride,
+                   const int64_t* n, int32_t B, int32_t H_I, int32_t d_I, int64_t n_max, int32_t P,
+                   int32_t* pool_out, void* ws, size_t ws_bytes, int32_t* d_status, void* stream) {
+  if (B < 0 || n_max < 0 || kbar_seq_stride < 0) return CSA2_ERR_INVALID_ARG;
+  if (!index_dims_ok(H_I, d_I) || !topk_k_ok(P) || n_max > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!qI || !w || !kbar || !n || !pool_out || !aligned16(qI) || !aligned16(kbar)) return CSA2_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, ws_form_pool(B, n_max))) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return pool_indexer(qI, w, kbar, kbar_seq_stride, n, B, H_I, d_I, n_max, P, pool_out, ws, d_status,
+                      static_cast<cudaStream_t>(stream));
+}
+
+int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                       const int64_t* n, const int32_t* pool, int32_t P, int32_t B, int32_t H_I,
+                       int32_t d_I, int32_t k, int32_t* idx_out, void* ws, size_t ws_bytes,
+                       int32_t* d_status, void* stream) {
+  if (B < 0 || P < 0 || kI_seq_stride < 0) return CSA2_ERR_INVALID_ARG;
+  if (!index_dims_ok(H_I, d_I) || !topk_k_ok(k) || P > kMaxTopK) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!qI || !w || !kI || !n || !pool || !idx_out || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, ws_reindex(B, P))) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return reindex_indexer(qI, w, kI, kI_seq_stride, n, pool, P, B, H_I, d_I, k, idx_out, ws, d_status,
+                         static_cast<cudaStream_t>(stream), nullptr, nullptr);
+}
+
+int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d, const uint8_t* codes,
+                     const uint8_t* scales, int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx,
+                     int32_t k, const void* swa, int64_t swa_seq_stride, int32_t W,
+                     const int32_t* swa_len, float softmax_scale, void* out, void* ws, size_t ws_bytes,
+                     int32_t* d_status, void* stream) {
+  if (B < 0 || k < 0 || W < 0 || kv_seq_stride < 0 || swa_seq_stride < 0 || n_cap < 0) return CSA2_ERR_INVALID_ARG;
+  if (d != 512 || (H != 16 && H != 32 && H != 48 && H != 64) || W > 128 || k > 4096)
+    return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!q || !out || !swa_len || (k > 0 && (!codes || !scales || !idx)) || (W > 0 && !swa))
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || (codes && !aligned16(codes)) || (scales && !aligned16(scales)) ||
+      (swa && !aligned16(swa)))
+    return CSA2_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, attn_ws_bytes(B, H, k, W))) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return launch_sparse_attn(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
+                            swa_len, softmax_scale, out, ws, d_status, static_cast<cudaStream_t>(stream));
+}
+
+static cudaEvent_t group_event(const csa2_group_args* a, int i) {
+  if (a->events == nullptr || i >= a->n_events) return nullptr;
+  return static_cast<cudaEvent_t>(a->events[i]);
+}
+
+int csa2_layer_group(const csa2_group_args* a, void* stream) {
+  if (!a) return CSA2_ERR_INVALID_ARG;
+  if (a->mode != CSA2_MODE_FULL && a->mode != CSA2_MODE_REINDEX) return CSA2_ERR_INVALID_ARG;
+  if (a->n_reuse < 0 || !a->q_layers || !a->swa_layers || !a->out_layers || !a->idx) return CSA2_ERR_INVALID_ARG;
+  if (a->B < 0 || a->n_max < 0 || a->n_max > a->n_cap || a->n_max > 0x7FFFFFFF) return CSA2_ERR_INVALID_ARG;
+  if (a->B == 0) return CSA2_OK;
+  if (!a->n || !a->codes || !a->scales || !a->kI || !a->qI || !a->w || !a->swa_len) return CSA2_ERR_INVALID_ARG;
+  if ((a->form_pool || a->mode == CSA2_MODE_REINDEX) && !a->pool) return CSA2_ERR_INVALID_ARG;
+  if (a->form_pool && !a->kbar) return CSA2_ERR_INVALID_ARG;
+  if (!index_dims_ok(a->H_I, a->d_I) || !topk_k_ok(a->k) || a->P < 0 || a->P > kMaxTopK ||
+      (a->form_pool && a->P < 1) || a->d != 512 || a->W < 0 || a->W > 128 ||
+      (a->H != 16 && a->H != 32 && a->H != 48 && a->H != 64))
+    return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a->qI) || !aligned16(a->kI) || (a->kbar && !aligned16(a->kbar))) return CSA2_ERR_INVALID_ARG;
+  const size_t need = csa2_workspace_size(CSA2_OP_LAYER_GROUP, a->B, a->n_cap, a->k, a->P, a->H);
+  if (!ws_ok(a->ws, a->ws_bytes, need)) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t nbc = (a->n_cap + kBlock - 1) / kBlock;
+  const uint8_t* qp = a->qI_pool ? a->qI_pool : a->qI;
+  const float* wp = a->w_pool ? a->w_pool : a->w;
+  // events: [0] indexer scan begins, [1] scan ends, [2] Top-K (and pool) done,
+  // [3 + l] attention of layer l done
+  if (a->mode == CSA2_MODE_FULL) {
+    rc = full_indexer(a->qI, a->w, a->kI, a->n_cap, a->n, a->B, a->H_I, a->d_I, a->n_max, a->k, a->idx, nullptr,
+                      a->ws, a->d_status, s, group_event(a, 0), group_event(a, 1));
+    if (rc == CSA2_OK && a->form_pool)
+      rc = pool_indexer(qp, wp, a->kbar, nbc, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
+                        a->d_status, s);
+  } else {
+    if ((rc = rec(group_event(a, 0), s)) != CSA2_OK) return rc;
+    if (a->form_pool)
+      rc = pool_indexer(qp, wp, a->kbar, nbc, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
+                        a->d_status, s);
+    if (rc == CSA2_OK)
+      rc = reindex_indexer(a->qI, a->w, a->kI, a->n_cap, a->n, a->pool, a->P, a->B, a->H_I, a->d_I, a->k,
+                           a->idx, a->ws, a->d_status, s, nullptr, group_event(a, 1));
+  }
+  if (rc != CSA2_OK) return rc;
+  if ((rc = rec(group_event(a, 2), s)) != CSA2_OK) return rc;
+  for (int l = 0; l <= a->n_reuse; ++l) {
+    if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
+    rc = launch_sparse_attn(a->q_layers[l], a->B, a->H, a->codes, a->scales, a->n_cap, a->n_cap, a->idx, a->k,
+                            a->swa_layers[l], a->W, a->W, a->swa_len, a->softmax_scale, a->out_layers[l], a->ws,
+                            a->d_status, s);
+    if (rc != CSA2_OK) return rc;
+    if ((rc = rec(group_event(a, 3 + l), s)) != CSA2_OK) return rc;
+  }
+  return CSA2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,130 @@
+// common.cuh — shared device helpers of libcsa2 (sm_103a).
+//
+// PTX wrappers for the conversions and tensor-core instructions the kernels
+// use, the order-preserving float key used by Top-K, and the host-side
+// launch bookkeeping. Nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+constexpr int kSMs = 148;              // B300: 2 dies x 74 SMs
+constexpr int kHistBins = 4096;        // level-0 Top-K histogram (12 key bits)
+constexpr int kCandCap = 8192;         // Top-K candidate buffer per row
+constexpr int kMaxTopK = 2048;
+constexpr int kBlock = 8;              // positions per pool block
+
+// ---- host bookkeeping ------------------------------------------------------
+void count_launch();
+int launch_status();                   // CSA2_OK or CSA2_ERR_CUDA after a launch
+
+// ---- device status ---------------------------------------------------------
+__device__ __forceinline__ void report(int32_t* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+// ---- order-preserving key of an fp32 score (larger score -> larger key) ----
+__device__ __forceinline__ uint32_t score_key(float s) {
+  uint32_t u = __float_as_uint(s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+// 64-bit composite: score desc, then position asc, as one unsigned order.
+__device__ __forceinline__ uint64_t cand_key(float s, int32_t pos) {
+  return ((uint64_t)score_key(s) << 32) | (uint32_t)(~(uint32_t)pos);
+}
+__device__ __forceinline__ int32_t cand_pos_of(uint64_t key) {
+  return (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
+}
+
+// ---- FP8 / FP4 conversions (hardware RNE, satfinite) -----------------------
+// Two fp32 -> E4M3 bytes; `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint8_t cvt_e4m3(float v) { return (uint8_t)(cvt_e4m3x2(v, 0.f) & 0xFF); }
+
+// Eight non-negative fp32 -> eight E2M1 codes packed low-nibble-first.
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float* f) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+  return r;
+}
+
+// E4M3 byte -> fp32 (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint8_t b) {
+  uint32_t h2;
+  uint16_t v = b;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+// One byte of two E2M1 codes -> f16x2 (low nibble -> low half), exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  uint16_t v = (uint16_t)byte;
+  asm("{\n .reg .b8 t, u;\n mov.b16 {t, u}, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "h"(v));
+  return r;
+}
+
+// ---- global loads ----------------------------------------------------------
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// ---- tensor-core MMA (warp-synchronous mma.sync) ----------------------------
+// D += A(16x32 e4m3, row) * B(32x8 e4m3, col), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- shared memory helpers -------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t smem_addr, const void* gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gptr));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
+
+}  // namespace csa2

@@ -1,0 +1,180 @@
+// index_scan.cu — the CSA2 indexer scan (Full, pool formation, Reindex).
+//
+// [CSA2] wire.sakhanda.co, "DeepSeek AI выпустила DeepSeek-V4.1-Flash ...",
+//        section "Сжатое разреженное внимание 2 (CSA2)": a Full layer
+//        projects indexer K and selects new Top-512 indices; a Reindex layer
+//        rescores the last Full layer's indexer K with its own indexer Q; the
+//        Full layer forms a pool of up to 2048 blocks of 8 positions so that
+//        Reindex layers score a bounded set. The score formula is not on the
+//        pages; this library computes s_t = sum_h w_h * relu(q_h . k_t) with
+//        one E4M3 key per position shared by all (<= 8) heads.
+//
+// Design (B300): the scan streams 64 or 128 bytes per position from HBM and
+// does 8 x d_I FP8 MACs per position, i.e. 8 MAC per byte. At ~6.7 TB/s
+// that is ~54 TMAC/s, above what the CUDA cores can sustain in fp32 FMA, so
+// the dot products run on the tensor cores: mma.sync m16n8k32 E4M3 x E4M3 ->
+// fp32 with the 16 rows of an m-tile as M and the (padded) 8 indexer heads
+// as N. A dot product is invariant under a common permutation of its
+// channels, so each thread loads whole 16-byte vectors of its rows straight
+// from global memory into A fragments (fully coalesced: a warp instruction
+// covers 8 rows x 64 contiguous bytes) and the query is loaded with the same
+// channel permutation into B fragments. The relu * w head sum is a
+// thread-local FMA pair plus two quad shuffles. The Top-K level-0 histogram
+// (12 high bits of the order-preserving score key) is accumulated in shared
+// memory and flushed once per CTA.
+#include "common.cuh"
+
+namespace csa2 {
+
+constexpr int kScanThreads = 256;
+constexpr int kScanTilesPerIter = 4;                 // m-tiles of 16 rows per warp iteration
+constexpr int kScanRowsPerWarpIter = 16 * kScanTilesPerIter;
+
+// SRC_POOL = false: rows are positions 0..n[b)-1 of the sequence.
+// SRC_POOL = true : slot s maps to position pool[b][s/8]*8 + s%8 (absent if
+//                   the block id is -1 or the position >= n[b]); cand_pos is
+//                   written for every slot so Top-K can skip absent ones.
+template <int DI, bool SRC_POOL>
+__global__ void __launch_bounds__(kScanThreads) k_index_scan(
+    const uint8_t* __restrict__ qI, const float* __restrict__ w, const uint8_t* __restrict__ kI,
+    int64_t kI_seq_stride, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max,
+    int64_t rows_per_cta, float* __restrict__ scores, int64_t scores_stride,
+    const int32_t* __restrict__ pool, int P, int32_t* __restrict__ cand_pos,
+    uint32_t* __restrict__ hist, int32_t* st) {
+  constexpr int CH = DI / 64;                         // 16-byte chunks per row per thread
+  __shared__ uint32_t sh_hist[kHistBins];
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+
+  int64_t nb = n[b];
+  nb = nb < 0 ? nb : (nb + len_div - 1) / len_div;   // len_div 8: positions -> pool blocks
+  if (nb > n_max || nb < 0) {
+    if (blockIdx.x == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+    nb = nb < 0 ? 0 : n_max;
+  }
+  const int64_t limit = SRC_POOL ? (int64_t)P * kBlock : nb;
+  const int64_t c0 = (int64_t)blockIdx.x * rows_per_cta;
+  const int64_t c1 = min(c0 + rows_per_cta, limit);
+  if (hist) {
+    for (int i = tid; i < kHistBins; i += kScanThreads) sh_hist[i] = 0;
+    __syncthreads();
+  }
+
+  // B fragments: head g, the thread's channel chunks {16t..16t+15, 64+16t..}
+  uint32_t qf[4 * CH];
+  {
+    const bool live = g < H_I;
+    const uint8_t* qrow = qI + ((int64_t)b * H_I + (live ? g : 0)) * DI;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + 64 * c + 16 * t) : make_uint4(0, 0, 0, 0);
+      qf[4 * c + 0] = v.x; qf[4 * c + 1] = v.y; qf[4 * c + 2] = v.z; qf[4 * c + 3] = v.w;
+    }
+  }
+  const float w0 = (2 * t < H_I) ? w[(int64_t)b * H_I + 2 * t] : 0.f;
+  const float w1 = (2 * t + 1 < H_I) ? w[(int64_t)b * H_I + 2 * t + 1] : 0.f;
+  const uint8_t* kseq = kI + (int64_t)b * kI_seq_stride * DI;
+  float* srow = scores + (int64_t)b * scores_stride;
+
+  for (int64_t base = c0 + (int64_t)warp * kScanRowsPerWarpIter; base < c1;
+       base += (int64_t)(kScanThreads / 32) * kScanRowsPerWarpIter) {
+    uint4 ra[kScanTilesPerIter][2][CH];
+    int64_t rpos[kScanTilesPerIter][2];
+#pragma unroll
+    for (int u = 0; u < kScanTilesPerIter; ++u) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int64_t slot = base + u * 16 + g + 8 * hh;
+        int64_t p = -1;
+        if (slot < c1) {
+          if (SRC_POOL) {
+            const int32_t blk = pool[(int64_t)b * P + (slot >> 3)];
+            const int64_t q = (int64_t)blk * kBlock + (slot & 7);
+            p = (blk >= 0 && q < nb) ? q : -1;
+          } else {
+            p = slot;
+          }
+        }
+        rpos[u][hh] = p;
+#pragma unroll
+        for (int c = 0; c < CH; ++c)
+          ra[u][hh][c] = (p >= 0) ? ldg_stream(kseq + p * DI + 64 * c + 16 * t) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kScanTilesPerIter; ++u) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < DI / 32; ++j) {
+        const uint4& r0 = ra[u][0][j >> 1];
+        const uint4& r1 = ra[u][1][j >> 1];
+        const uint32_t a0 = (j & 1) ? r0.z : r0.x, a2 = (j & 1) ? r0.w : r0.y;
+        const uint32_t a1 = (j & 1) ? r1.z : r1.x, a3 = (j & 1) ? r1.w : r1.y;
+        mma_e4m3_16832(acc, a0, a1, a2, a3, qf[2 * j], qf[2 * j + 1]);
+      }
+      float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
+      float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      if (t < 2) {
+        const int64_t slot = base + u * 16 + g + 8 * t;
+        const float sc = t ? s1 : s0;
+        const int64_t p = rpos[u][t];
+        if (slot < c1) {
+          if (SRC_POOL) {
+            cand_pos[(int64_t)b * scores_stride + slot] = (int32_t)p;
+            srow[slot] = sc;
+            if (hist && p >= 0) atomicAdd(&sh_hist[score_key(sc) >> 20], 1u);
+          } else {
+            srow[slot] = sc;
+            if (hist) atomicAdd(&sh_hist[score_key(sc) >> 20], 1u);
+          }
+        }
+      }
+    }
+  }
+  if (hist) {
+    __syncthreads();
+    uint32_t* gh = hist + (int64_t)b * kHistBins;
+    for (int i = tid; i < kHistBins; i += kScanThreads) {
+      const uint32_t v = sh_hist[i];
+      if (v) atomicAdd(gh + i, v);
+    }
+  }
+}
+
+// rows_per_cta: a multiple of the CTA's rows per iteration, sized so the
+// grid covers the machine a few times over.
+static int64_t scan_rows_per_cta(int B, int64_t rows) {
+  const int64_t step = (int64_t)(kScanThreads / 32) * kScanRowsPerWarpIter;  // 512
+  int64_t per = 4096;
+  while (per > step && (int64_t)B * ((rows + per - 1) / per) < 4 * kSMs) per /= 2;
+  return per;
+}
+
+int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+                      const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
+                      int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
+                      uint32_t* hist, int32_t* st, cudaStream_t s) {
+  const bool use_pool = pool != nullptr;
+  const int64_t rows = use_pool ? (int64_t)P * kBlock : n_max;
+  if (rows == 0 || B == 0) return CSA2_OK;
+  const int64_t per = scan_rows_per_cta(B, rows);
+  dim3 grid((unsigned)((rows + per - 1) / per), (unsigned)B);
+#define CSA2_SCAN(DI_, POOL_)                                                                   \
+  k_index_scan<DI_, POOL_><<<grid, kScanThreads, 0, s>>>(qI, w, kI, kI_seq_stride, n, len_div, H_I, n_max, \
+                                                         per, scores, scores_stride, pool, P,     \
+                                                         cand_pos, hist, st)
+  if (d_I == 128) {
+    if (use_pool) CSA2_SCAN(128, true); else CSA2_SCAN(128, false);
+  } else {
+    if (use_pool) CSA2_SCAN(64, true); else CSA2_SCAN(64, false);
+  }
+#undef CSA2_SCAN
+  count_launch();
+  return launch_status();
+}
+
+}  // namespace csa2

@@ -1,0 +1,218 @@
+// quantize.cu — cache writers: FP4 main-KV quantise/append, indexer-K append
+// with block means, sliding-window ring append.
+//
+// [FP4] wire.sakhanda.co, "DeepSeek AI выпустила DeepSeek-V4.1-Flash ...",
+//       section "FP4 KV, ограниченное повторное проигрывание и другие
+//       расширения": main KV stored as E2M1 with one E4M3 scale per 16
+//       channels and no global scale.
+// [CSA2] same page, section "Сжатое разреженное внимание 2 (CSA2)": the pool
+//       is built from blocks of 8 positions.
+// [CED] same page, section "Каузальный энкодер-декодер: вдвое меньший
+//       префилл": 128-token sliding window in every layer.
+//
+// All three writers are HBM-bound copies with a little arithmetic; one warp
+// owns one row so every load and store is a full 16-byte vector.
+#include "common.cuh"
+
+namespace csa2 {
+
+// One warp per bf16 row of 512 channels: lane l owns group l (channels
+// 16l..16l+15), i.e. one E4M3 scale and 8 bytes of codes.
+__global__ void __launch_bounds__(256) k_quantize_fp4(const uint4* __restrict__ x, int B, int64_t rows,
+                                                      const int64_t* __restrict__ pos,
+                                                      uint8_t* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales, int64_t n_cap,
+                                                      int32_t* st) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t total = (int64_t)B * rows;
+  for (int64_t r = (((int64_t)blockIdx.x * blockDim.x) + threadIdx.x) >> 5; r < total; r += nwarps) {
+    const int b = (int)(r / rows);
+    const int64_t i = r - (int64_t)b * rows;
+    const int64_t p = (pos ? pos[b] : 0) + i;
+    if (p < 0 || p >= n_cap) {
+      if (lane == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    // 512 bf16 = 64 uint4 per row; lane reads its two
+    const uint4 v0 = x[r * 64 + lane * 2];
+    const uint4 v1 = x[r * 64 + lane * 2 + 1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+    uint32_t sign_lo = 0, sign_hi = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      const uint32_t s0 = (w[j] >> 15) & 1u, s1 = (w[j] >> 31) & 1u;
+      if (j < 4) {
+        sign_lo |= (s0 << (8 * j + 3)) | (s1 << (8 * j + 7));
+      } else {
+        sign_hi |= (s0 << (8 * (j - 4) + 3)) | (s1 << (8 * (j - 4) + 7));
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    const uint8_t sc = cvt_e4m3(__fdiv_rn(amax, 6.0f));
+    const float s = e4m3_to_f32(sc);
+    uint32_t lo = 0, hi = 0;
+    if (s > 0.f) {
+      float m[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m[j] = __fdiv_rn(fabsf(f[j]), s);
+      lo = cvt_e2m1x8(m) | sign_lo;
+      hi = cvt_e2m1x8(m + 8) | sign_hi;
+    }
+    const int64_t row = (int64_t)b * n_cap + p;
+    *reinterpret_cast<uint2*>(codes + row * 256 + lane * 8) = make_uint2(lo, hi);
+    scales[row * 32 + lane] = sc;
+  }
+}
+
+// Copy E4M3 indexer-key rows into the cache: one thread per 16-byte chunk.
+__global__ void k_copy_index_rows(const uint8_t* __restrict__ k_new, int B, int64_t rows, int d_I,
+                                  const int64_t* __restrict__ pos, uint8_t* __restrict__ kI,
+                                  int64_t n_cap, int32_t* st) {
+  const int chunks = d_I / 16;
+  const int64_t total = (int64_t)B * rows * chunks;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / chunks;
+    const int c = (int)(e - r * chunks);
+    const int b = (int)(r / rows);
+    const int64_t i = r - (int64_t)b * rows;
+    const int64_t p = (pos ? pos[b] : 0) + i;
+    if (p < 0 || p >= n_cap) {
+      if (c == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const uint4 v = *reinterpret_cast<const uint4*>(k_new + r * d_I + c * 16);
+    *reinterpret_cast<uint4*>(kI + ((int64_t)b * n_cap + p) * d_I + c * 16) = v;
+  }
+}
+
+// Mean key of block j of one sequence over positions [8j, end): exact fp32
+// sum of E4M3 values (at most 8 terms, magnitudes 2^-9 .. 448, so at most 21
+// significant bits), IEEE division by the count, E4M3 RNE with saturation.
+// One warp per block; lane l owns channels 4l..4l+3.
+__device__ __forceinline__ void block_mean_warp(const uint8_t* __restrict__ kI_seq,
+                                                uint8_t* __restrict__ kbar_seq, int64_t j,
+                                                int64_t end, int d_I, int lane) {
+  const int64_t beg = j * kBlock;
+  const float cnt = (float)(end - beg);
+  for (int c = lane * 4; c < d_I; c += 128) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int64_t t = beg; t < end; ++t) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(kI_seq + t * d_I + c);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[u] += e4m3_to_f32((uint8_t)(v >> (8 * u)));
+    }
+    const uint16_t lo = cvt_e4m3x2(__fdiv_rn(acc[0], cnt), __fdiv_rn(acc[1], cnt));
+    const uint16_t hi = cvt_e4m3x2(__fdiv_rn(acc[2], cnt), __fdiv_rn(acc[3], cnt));
+    *reinterpret_cast<uint32_t*>(kbar_seq + j * d_I + c) = (uint32_t)lo | ((uint32_t)hi << 16);
+  }
+}
+
+// Blocks touched by an append of `rows` positions starting at pos[b]: the
+// mean covers the block start through the last appended position.
+__global__ void k_block_means_append(const uint8_t* __restrict__ kI, int B, int64_t rows, int d_I,
+                                     const int64_t* __restrict__ pos, uint8_t* __restrict__ kbar,
+                                     int64_t n_cap, int64_t touched) {
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int64_t jj = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (jj >= touched) return;
+  const int64_t p0 = pos ? pos[b] : 0;
+  const int64_t last = p0 + rows - 1;
+  if (p0 < 0 || last >= n_cap) return;  // the copy kernel reported it
+  const int64_t j = p0 / kBlock + jj;
+  if (j * kBlock > last) return;
+  const int64_t end = min((j + 1) * kBlock, last + 1);
+  const int64_t nbc = (n_cap + kBlock - 1) / kBlock;
+  block_mean_warp(kI + (int64_t)b * n_cap * d_I, kbar + (int64_t)b * nbc * d_I, j, end, d_I, lane);
+}
+
+// Every block of positions [0, n[b]).
+__global__ void k_block_means_all(const uint8_t* __restrict__ kI, int d_I,
+                                  const int64_t* __restrict__ n, int64_t n_cap,
+                                  uint8_t* __restrict__ kbar, int32_t* st) {
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31;
+  const int64_t j = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int64_t nb = n[b];
+  if (nb > n_cap) {
+    if (j == 0 && lane == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+    nb = n_cap;
+  }
+  if (j * kBlock >= nb) return;
+  const int64_t end = min((j + 1) * kBlock, nb);
+  const int64_t nbc = (n_cap + kBlock - 1) / kBlock;
+  block_mean_warp(kI + (int64_t)b * n_cap * d_I, kbar + (int64_t)b * nbc * d_I, j, end, d_I, lane);
+}
+
+// One warp per sequence copies its new sliding-window row into slot pos % W.
+__global__ void k_append_swa(const uint4* __restrict__ x, int B, int d, const int64_t* __restrict__ pos,
+                             uint4* __restrict__ swa, int W) {
+  const int b = (int)(((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (b >= B) return;
+  int64_t slot = pos[b] % W;
+  if (slot < 0) slot += W;
+  const int chunks = d / 8;  // bf16: 8 per 16 bytes
+  for (int c = lane; c < chunks; c += 32)
+    swa[((int64_t)b * W + slot) * chunks + c] = x[(int64_t)b * chunks + c];
+}
+
+// ---- host launchers -----------------------------------------------------
+int launch_quantize_fp4(const void* x, int B, int64_t rows, const int64_t* pos, uint8_t* codes,
+                        uint8_t* scales, int64_t n_cap, int32_t* st, cudaStream_t s) {
+  const int64_t total = (int64_t)B * rows;
+  const int64_t warps = total;
+  int64_t blocks = (warps + 7) / 8;
+  blocks = blocks < kSMs * 16 ? blocks : kSMs * 16;
+  if (blocks < 1) return CSA2_OK;
+  k_quantize_fp4<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), B, rows, pos,
+                                                  codes, scales, n_cap, st);
+  count_launch();
+  return launch_status();
+}
+
+int launch_append_indexer_k(const uint8_t* k_new, int B, int64_t rows, int d_I, const int64_t* pos,
+                            uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st,
+                            cudaStream_t s) {
+  const int64_t total = (int64_t)B * rows * (d_I / 16);
+  if (total == 0) return CSA2_OK;
+  int64_t blocks = (total + 255) / 256;
+  blocks = blocks < kSMs * 16 ? blocks : kSMs * 16;
+  k_copy_index_rows<<<(unsigned)blocks, 256, 0, s>>>(k_new, B, rows, d_I, pos, kI, n_cap, st);
+  count_launch();
+  int rc = launch_status();
+  if (rc != CSA2_OK || kbar == nullptr) return rc;
+  const int64_t touched = (rows + kBlock - 1) / kBlock + 1;
+  dim3 grid((unsigned)((touched + 7) / 8), (unsigned)B);
+  k_block_means_append<<<grid, 256, 0, s>>>(kI, B, rows, d_I, pos, kbar, n_cap, touched);
+  count_launch();
+  return launch_status();
+}
+
+int launch_block_means(const uint8_t* kI, int B, int d_I, const int64_t* n, int64_t n_max,
+                       int64_t n_cap, uint8_t* kbar, int32_t* st, cudaStream_t s) {
+  const int64_t nb = (n_max + kBlock - 1) / kBlock;
+  if (nb == 0 || B == 0) return CSA2_OK;
+  dim3 grid((unsigned)((nb + 7) / 8), (unsigned)B);
+  k_block_means_all<<<grid, 256, 0, s>>>(kI, d_I, n, n_cap, kbar, st);
+  count_launch();
+  return launch_status();
+}
+
+int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa, int W,
+                      cudaStream_t s) {
+  const int64_t threads = (int64_t)B * 32;
+  k_append_swa<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+      reinterpret_cast<const uint4*>(x), B, d, pos, reinterpret_cast<uint4*>(swa), W);
+  count_launch();
+  return launch_status();
+}
+
+}  // namespace csa2

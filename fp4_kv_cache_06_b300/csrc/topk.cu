@@ -1,0 +1,383 @@
+// topk.cu — deterministic Top-K selection for the CSA2 indexer.
+//
+// [CSA2] wire.sakhanda.co, "DeepSeek AI выпустила DeepSeek-V4.1-Flash ...",
+//        section "Сжатое разреженное внимание 2 (CSA2)": Full selects new
+//        Top-512 indices; Reindex selects again among the pool; the pool
+//        itself keeps the best 2048 blocks.
+//
+// Order: score descending, then position ascending. Each candidate becomes
+// a unique 64-bit key (order-preserving score bits << 32 | ~position), so the
+// k best are exactly the k largest keys and the result does not depend on
+// the order in which threads or CTAs visit the candidates.
+//
+// Pipeline per row (three launches; the first is fused into the indexer
+// scan when the scan runs just before):
+//   1. histogram of the 12 high key bits (4096 bins) over the row;
+//   2. compaction: every CTA derives the same threshold bin from the
+//      histogram and appends the candidates at or above it (at most
+//      kCandCap) to the row's candidate buffer; if more than kCandCap would
+//      qualify the row is flagged and left to step 3's slow path;
+//   3. one CTA per row: exact radix select of the k-th largest key over the
+//      compacted candidates in shared memory (or, for a flagged row, over the
+//      whole row in global memory), then a bitonic sort of the chosen
+//      positions, -1 padding.
+#include "common.cuh"
+
+namespace csa2 {
+
+struct TopkHdr {
+  uint32_t cnt;       // candidates appended by the compaction
+  uint32_t overflow;  // 1 = more than kCandCap would qualify: use the slow path
+  uint32_t pad[2];
+};
+
+// Workspace layout (all offsets 256-byte aligned):
+//   hist [B][kHistBins] u32 | hdr [B] TopkHdr | cand [B][kCandCap] u64
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t topk_ws_bytes(int B) {
+  return align256((size_t)B * kHistBins * 4) + align256((size_t)B * sizeof(TopkHdr)) +
+         align256((size_t)B * kCandCap * 8);
+}
+struct TopkWs {
+  uint32_t* hist;
+  TopkHdr* hdr;
+  uint64_t* cand;
+};
+static TopkWs topk_ws(void* ws, int B) {
+  char* p = static_cast<char*>(ws);
+  TopkWs r;
+  r.hist = reinterpret_cast<uint32_t*>(p);
+  p += align256((size_t)B * kHistBins * 4);
+  r.hdr = reinterpret_cast<TopkHdr*>(p);
+  p += align256((size_t)B * sizeof(TopkHdr));
+  r.cand = reinterpret_cast<uint64_t*>(p);
+  return r;
+}
+uint32_t* topk_ws_hist(void* ws) { return static_cast<uint32_t*>(ws); }
+
+constexpr int kTkThreads = 256;
+
+// Candidates of row b: the first ceil(n[b] / len_div) entries, at most n_max
+// (n == NULL: every row has n_max entries).
+__device__ __forceinline__ int64_t row_len(const int64_t* n, int b, int len_div, int64_t n_max) {
+  if (n == nullptr) return n_max;
+  int64_t v = n[b];
+  v = v <= 0 ? 0 : (v + len_div - 1) / len_div;
+  return v < n_max ? v : n_max;
+}
+
+// ---- step 1 (standalone form) --------------------------------------------
+__global__ void __launch_bounds__(kTkThreads) k_topk_hist(const float* __restrict__ scores,
+                                                          const int32_t* __restrict__ cand_pos,
+                                                          int64_t stride, const int64_t* __restrict__ n,
+                                                          int len_div, int64_t n_max, int64_t per,
+                                                          uint32_t* __restrict__ hist) {
+  __shared__ uint32_t sh[kHistBins];
+  const int b = blockIdx.y;
+  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = 0;
+  __syncthreads();
+  const int64_t nb = row_len(n, b, len_div, n_max);
+  const int64_t c0 = (int64_t)blockIdx.x * per, c1 = min(c0 + per, nb);
+  const float* s = scores + (int64_t)b * stride;
+  const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
+  for (int64_t i = c0 + threadIdx.x; i < c1; i += kTkThreads) {
+    if (cp && cp[i] < 0) continue;
+    atomicAdd(&sh[score_key(s[i]) >> 20], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads)
+    if (sh[i]) atomicAdd(hist + (int64_t)b * kHistBins + i, sh[i]);
+}
+
+// Threshold bin: the highest bin v with (count of keys in bins >= v) >= k,
+// or bin 0 when the row has fewer than k keys. Also returns that count.
+// 256 threads, each owning 16 consecutive bins counted from the top.
+__device__ void find_threshold_bin(const uint32_t* __restrict__ h, int k, int* out_bin,
+                                   uint32_t* out_ge) {
+  __shared__ uint32_t part[kTkThreads];
+  __shared__ int s_bin;
+  __shared__ uint32_t s_ge;
+  const int tid = threadIdx.x;
+  const int hi = kHistBins - 16 * tid;  // bins [hi-16, hi)
+  uint32_t loc = 0;
+#pragma unroll
+  for (int i = 1; i <= 16; ++i) loc += h[hi - i];
+  part[tid] = loc;
+  if (tid == 0) { s_bin = 0; s_ge = 0xFFFFFFFFu; }
+  __syncthreads();
+  // inclusive scan over threads (Hillis-Steele in shared memory)
+  for (int off = 1; off < kTkThreads; off <<= 1) {
+    const uint32_t v = tid >= off ? part[tid - off] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  const uint32_t incl = part[tid], excl = incl - loc;
+  const uint32_t total = part[kTkThreads - 1];
+  if (total < (uint32_t)k) {
+    if (tid == 0) { s_bin = 0; s_ge = total; }
+  } else if (excl < (uint32_t)k && incl >= (uint32_t)k) {
+    uint32_t run = excl;
+    for (int i = 1; i <= 16; ++i) {
+      run += h[hi - i];
+      if (run >= (uint32_t)k) { s_bin = hi - i; s_ge = run; break; }
+    }
+  }
+  __syncthreads();
+  *out_bin = s_bin;
+  *out_ge = s_ge;
+}
+
+// ---- step 2 ----------------------------------------------------------------
+__global__ void __launch_bounds__(kTkThreads) k_topk_compact(const float* __restrict__ scores,
+                                                             const int32_t* __restrict__ cand_pos,
+                                                             int64_t stride, const int64_t* __restrict__ n,
+                                                             int len_div, int64_t n_max, int64_t per, int k,
+                                                             const uint32_t* __restrict__ hist,
+                                                             TopkHdr* __restrict__ hdr,
+                                                             uint64_t* __restrict__ cand) {
+  __shared__ uint32_t sh[kHistBins];
+  const int b = blockIdx.y;
+  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = hist[(int64_t)b * kHistBins + i];
+  __syncthreads();
+  int vbin;
+  uint32_t ge;
+  find_threshold_bin(sh, k, &vbin, &ge);
+  if (ge > (uint32_t)kCandCap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) hdr[b].overflow = 1u;
+    return;
+  }
+  const int64_t nb = row_len(n, b, len_div, n_max);
+  const int64_t c0 = (int64_t)blockIdx.x * per, c1 = min(c0 + per, nb);
+  const float* s = scores + (int64_t)b * stride;
+  const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
+  uint64_t* out = cand + (int64_t)b * kCandCap;
+  const int lane = threadIdx.x & 31;
+  for (int64_t i0 = c0; i0 < c1; i0 += kTkThreads) {
+    const int64_t i = i0 + threadIdx.x;
+    bool take = false;
+    uint64_t key = 0;
+    if (i < c1) {
+      const int32_t p = cp ? cp[i] : (int32_t)i;
+      const float v = s[i];
+      if (p >= 0 && (int)(score_key(v) >> 20) >= vbin) {
+        take = true;
+        key = cand_key(v, p);
+      }
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, take);
+    if (m) {
+      uint32_t basei = 0;
+      const int leader = __ffs(m) - 1;
+      if (lane == leader) basei = atomicAdd(&hdr[b].cnt, (uint32_t)__popc(m));
+      basei = __shfl_sync(0xffffffffu, basei, leader);
+      if (take) {
+        const uint32_t slot = basei + __popc(m & ((1u << lane) - 1u));
+        if (slot < (uint32_t)kCandCap) out[slot] = key;  // always true: ge <= kCandCap
+      }
+    }
+  }
+}
+
+// ---- step 3 ----------------------------------------------------------------
+constexpr int kFinThreads = 1024;
+
+// Key sources for the radix select.
+struct SmemKeys {
+  const uint64_t* keys;
+  int cnt;
+  __device__ int64_t size() const { return cnt; }
+  __device__ bool get(int64_t i, uint64_t& key) const { key = keys[i]; return true; }
+};
+struct RowKeys {
+  const float* s;
+  const int32_t* cp;
+  int64_t cnt;
+  __device__ int64_t size() const { return cnt; }
+  __device__ bool get(int64_t i, uint64_t& key) const {
+    const int32_t p = cp ? cp[i] : (int32_t)i;
+    if (p < 0) return false;
+    key = cand_key(s[i], p);
+    return true;
+  }
+};
+
+// Exact key of the k-th largest among the source's keys (all distinct);
+// requires at least k keys. MSD radix, 8 bits per pass.
+template <class Src>
+__device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
+  __shared__ uint64_t s_prefix;
+  __shared__ int s_remaining;
+  const int tid = threadIdx.x;
+  uint64_t prefix = 0, mask = 0;
+  int remaining = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kFinThreads) h256[i] = 0;
+    __syncthreads();
+    const int64_t m = src.size();
+    for (int64_t i = tid; i < m; i += kFinThreads) {
+      uint64_t key;
+      if (src.get(i, key) && (key & mask) == prefix) atomicAdd(&h256[(key >> shift) & 255], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // lane l owns digits [255-8l-7, 255-8l], counted from the top
+      uint32_t loc = 0;
+      for (int j = 0; j < 8; ++j) loc += h256[255 - 8 * tid - j];
+      uint32_t incl = loc;
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (tid >= off) incl += v;
+      }
+      const uint32_t excl = incl - loc;
+      if (excl < (uint32_t)remaining && incl >= (uint32_t)remaining) {
+        uint32_t run = excl;
+        for (int j = 0; j < 8; ++j) {
+          const int dgt = 255 - 8 * tid - j;
+          const uint32_t c = h256[dgt];
+          if (run + c >= (uint32_t)remaining) {
+            s_prefix = prefix | ((uint64_t)dgt << shift);
+            s_remaining = remaining - (int)run;
+            break;
+          }
+          run += c;
+        }
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    remaining = s_remaining;
+    mask |= (uint64_t)255 << shift;
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Bitonic sort of sel[0..np) ascending (np a power of two, padded with INT_MAX).
+__device__ void bitonic_sort_i32(int32_t* sel, int np) {
+  for (int size = 2; size <= np; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < np / 2; i += kFinThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0);
+        const int32_t a = sel[lo], c = sel[hi];
+        if ((a > c) == up) { sel[lo] = c; sel[hi] = a; }
+      }
+    }
+  }
+  __syncthreads();
+}
+
+template <class Src>
+__device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t* __restrict__ out,
+                                 uint32_t* h256, int32_t* sel) {
+  __shared__ uint32_t s_cnt;
+  const int tid = threadIdx.x;
+  uint64_t thr = 0;
+  if (n_keys > k) thr = radix_kth(src, k, h256);
+  if (tid == 0) s_cnt = 0;
+  int np = 1;
+  while (np < k) np <<= 1;
+  for (int i = tid; i < np; i += kFinThreads) sel[i] = 0x7FFFFFFF;
+  __syncthreads();
+  const int64_t m = src.size();
+  for (int64_t i = tid; i < m; i += kFinThreads) {
+    uint64_t key;
+    if (src.get(i, key) && key >= thr) {
+      const uint32_t slot = atomicAdd(&s_cnt, 1u);
+      if (slot < (uint32_t)k) sel[slot] = cand_pos_of(key);
+    }
+  }
+  __syncthreads();
+  const int cnt = (int)min(s_cnt, (uint32_t)k);
+  bitonic_sort_i32(sel, np);
+  for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? sel[i] : -1;
+}
+
+__global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restrict__ scores,
+                                                            const int32_t* __restrict__ cand_pos,
+                                                            int64_t stride, const int64_t* __restrict__ n,
+                                                            int len_div, int64_t n_max, int k,
+                                                            const TopkHdr* __restrict__ hdr,
+                                                            const uint64_t* __restrict__ cand,
+                                                            int32_t* __restrict__ idx_out) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                 // kCandCap
+  uint32_t* h256 = reinterpret_cast<uint32_t*>(keys + kCandCap);      // 256
+  int32_t* sel = reinterpret_cast<int32_t*>(h256 + 256);              // kMaxTopK
+  const int b = blockIdx.x;
+  int32_t* out = idx_out + (int64_t)b * k;
+  const int64_t nb = row_len(n, b, len_div, n_max);
+  if (hdr[b].overflow) {
+    // slow path: count the row's present candidates, then select over global memory
+    __shared__ uint32_t s_valid;
+    if (threadIdx.x == 0) s_valid = 0;
+    __syncthreads();
+    const float* s = scores + (int64_t)b * stride;
+    const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
+    uint32_t loc = 0;
+    for (int64_t i = threadIdx.x; i < nb; i += kFinThreads) loc += (cp == nullptr || cp[i] >= 0);
+    atomicAdd(&s_valid, loc);
+    __syncthreads();
+    RowKeys src{s, cp, nb};
+    select_and_write(src, k, (int64_t)s_valid, out, h256, sel);
+    return;
+  }
+  const int cnt = (int)min(hdr[b].cnt, (uint32_t)kCandCap);
+  for (int i = threadIdx.x; i < cnt; i += kFinThreads) keys[i] = cand[(int64_t)b * kCandCap + i];
+  __syncthreads();
+  SmemKeys src{keys, cnt};
+  select_and_write(src, k, cnt, out, h256, sel);
+}
+
+int topk_final_smem() { return kCandCap * 8 + 256 * 4 + kMaxTopK * 4; }
+
+// ---- host ------------------------------------------------------------------
+static int64_t tk_rows_per_cta(int B, int64_t rows) {
+  int64_t per = 16384;
+  while (per > 1024 && (int64_t)B * ((rows + per - 1) / per) < 4 * kSMs) per /= 2;
+  return per;
+}
+
+// Zero the histogram and headers of B rows (before the scan or step 1).
+int topk_prepare(void* ws, int B, cudaStream_t s) {
+  const size_t bytes = align256((size_t)B * kHistBins * 4) + align256((size_t)B * sizeof(TopkHdr));
+  if (cudaMemsetAsync(ws, 0, bytes, s) != cudaSuccess) return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}
+
+// Steps 1 (unless the histogram is already in the workspace), 2 and 3.
+int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, const int64_t* n,
+                int len_div, int B, int64_t n_max, int k, int32_t* idx_out, void* ws, bool hist_ready,
+                cudaStream_t s) {
+  if (B == 0) return CSA2_OK;
+  TopkWs w = topk_ws(ws, B);
+  int rc;
+  const int64_t per = tk_rows_per_cta(B, n_max);
+  dim3 grid((unsigned)((n_max + per - 1) / per > 0 ? (n_max + per - 1) / per : 1), (unsigned)B);
+  if (!hist_ready) {
+    if ((rc = topk_prepare(ws, B, s)) != CSA2_OK) return rc;
+    k_topk_hist<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, w.hist);
+    count_launch();
+    if ((rc = launch_status()) != CSA2_OK) return rc;
+  }
+  k_topk_compact<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, k, w.hist, w.hdr,
+                                             w.cand);
+  count_launch();
+  if ((rc = launch_status()) != CSA2_OK) return rc;
+  k_topk_final<<<B, kFinThreads, topk_final_smem(), s>>>(scores, cand_pos, stride, n, len_div, n_max, k, w.hdr,
+                                                          w.cand, idx_out);
+  count_launch();
+  return launch_status();
+}
+
+int topk_init_attributes() {
+  if (cudaFuncSetAttribute(k_topk_final, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           topk_final_smem()) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  return CSA2_OK;
+}
+
+}  // namespace csa2

@@ -1,0 +1,273 @@
+/*
+ * csa2.h — C ABI of libcsa2.so, the B300 (sm_103a) hot path of Compressed
+ * Sparse Attention 2 (CSA2) over a shared main-KV cache held in FP4.
+ *
+ * Page citations used below:
+ *  [CSA2] wire.sakhanda.co, "DeepSeek AI выпустила DeepSeek-V4.1-Flash с
+ *         контекстом в 1 млн токенов, KV-кэшем FP4 и повторным
+ *         использованием внимания между слоями", section "Сжатое разреженное
+ *         внимание 2 (CSA2)": layer modes Full / Reindex / Reuse, Top-512,
+ *         each layer's own main Q and SWA KV, the hierarchical pool of up to
+ *         2048 blocks x 8 positions formed by the Full layer.
+ *  [FP4]  same page, section "FP4 KV, ограниченное повторное проигрывание и
+ *         другие расширения": main KV in E2M1 with one E4M3 scale per 16
+ *         channels, without NVFP4's global scale.
+ *  [CED]  same page, section "Каузальный энкодер-декодер: вдвое меньший
+ *         префилл": every layer keeps 128-token sliding-window attention.
+ *  [TG]   tgviewer.app, "DeepSeek-V4.1-Flash: Frontier Agents on a Smaller
+ *         Memory Budget", CSA2 bullet: sharing Top-K indices removes
+ *         re-scoring the whole history.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    never allocates. Scratch memory comes from a caller-provided workspace
+ *    of at least csa2_workspace_size(...) bytes, 256-byte aligned.
+ *  - Every tensor base must be 16-byte aligned; rows are packed (no padding)
+ *    unless a stride argument says otherwise. Strides are in ROWS.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns without synchronising the host; results are valid
+ *    once the stream reaches that point. Calls are capturable in CUDA graphs
+ *    (no host synchronisation, no allocation; memsets are async).
+ *  - The return value is a csa2_status. Host-side validation failures
+ *    return before enqueuing anything. Device-side checks (an index or a
+ *    length out of range) never trap: the offending access is skipped and,
+ *    when `d_status` (a device int32, caller-zeroed) is non-NULL, the first
+ *    failing code is written there with an atomic compare-and-swap.
+ *  - Formats: bf16 tensors are IEEE bfloat16; E4M3 tensors are raw bytes of
+ *    the OCP FP8 E4M3 ("fn") format; the FP4 main-KV cache is two planes,
+ *    `codes` [.., d/2] (two E2M1 codes per byte, channel 2i in the low
+ *    nibble, bit 3 of a code = sign) and `scales` [.., d/16] (E4M3).
+ *  - Layout symbols: B sequences (or prefill queries), n positions, d = 512
+ *    main dim, H main query heads (multiple of 16, <= 64), H_I <= 8 indexer
+ *    heads, d_I in {64, 128} indexer dim, k <= 2048 Top-K, W <= 128 window.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,      /* NULL / misaligned pointer, bad value      */
+  CSA2_ERR_UNSUPPORTED_SHAPE = 2,/* a size outside what the kernels support  */
+  CSA2_ERR_WORKSPACE = 3,        /* workspace missing or too small           */
+  CSA2_ERR_CUDA = 4,             /* a CUDA launch or memset failed           */
+  CSA2_ERR_TIMEOUT = 5,          /* a bounded device wait gave up            */
+  CSA2_ERR_DEVICE_BOUNDS = 6     /* (device) an index/length was out of range */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+CSA2_API const char* csa2_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+CSA2_API int csa2_version(void);
+
+/* Number of kernel launches this process has issued through the library
+ * (host-side counter; graph replays of captured launches are not counted). */
+CSA2_API uint64_t csa2_launch_count(void);
+
+/* ---- workspace sizing -------------------------------------------------- */
+enum csa2_op {
+  CSA2_OP_TOPK = 1,          /* csa2_topk                                  */
+  CSA2_OP_INDEX_FULL = 2,    /* csa2_index_full (scores + Top-K)           */
+  CSA2_OP_INDEX_REINDEX = 3, /* csa2_index_reindex                         */
+  CSA2_OP_FORM_POOL = 4,     /* csa2_form_pool                             */
+  CSA2_OP_SPARSE_ATTN = 5,   /* csa2_sparse_attn (split-K partials)        */
+  CSA2_OP_LAYER_GROUP = 6    /* csa2_layer_group (max of the above)        */
+};
+
+/* Bytes of workspace an op needs for B rows of at most n_max candidates,
+ * Top-k, pool P blocks and H heads (arguments an op does not use are
+ * ignored). Returns 0 for an unknown op. */
+CSA2_API size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k,
+                           int32_t P, int32_t H);
+
+/* ---- a1: FP4 quantise / append [FP4] ----------------------------------- */
+/* Quantise bf16 main-KV rows to E2M1 codes with one E4M3 scale per 16
+ * channels (no global scale) and store them in the cache. Per group of 16
+ * channels: scale = E4M3(amax / 6) rounded to nearest even with saturation;
+ * code_c = sign(x_c) | E2M1(|x_c| / scale) rounded to nearest even with
+ * saturation at 6; a group whose scale is zero stores +0 codes. The result
+ * is bit-exact (IEEE fp32 division, hardware RNE conversions).
+ *   x      [B][rows][d] bf16
+ *   pos    [B] int64 device (NULL = all zero): row r of sequence b goes to
+ *          cache position pos[b] + r
+ *   codes  [B][n_cap][d/2] u8, scales [B][n_cap][d/16] u8
+ * Rows whose position is >= n_cap are skipped (CSA2_ERR_DEVICE_BOUNDS). */
+CSA2_API int csa2_quantize_kv_fp4(const void* x, int32_t B, int64_t rows, int32_t d,
+                         const int64_t* pos, uint8_t* codes, uint8_t* scales,
+                         int64_t n_cap, int32_t* d_status, void* stream);
+
+/* ---- a2: indexer-K append + block means [CSA2] ------------------------- */
+/* Copy E4M3 indexer-key rows into the cache and refresh the mean key of
+ * every aligned 8-position block they touch (the pool is formed over
+ * blocks of 8 positions). A block's mean covers its positions from the
+ * block start through the last appended position: the exact fp32 sum of
+ * the present keys divided by their count, rounded to E4M3 (RNE, sat).
+ *   k_new [B][rows][d_I] u8; pos [B] int64 device (NULL = 0)
+ *   kI    [B][n_cap][d_I] u8; kbar [B][ceil(n_cap/8)][d_I] u8 */
+CSA2_API int csa2_append_indexer_k(const uint8_t* k_new, int32_t B, int64_t rows,
+                          int32_t d_I, const int64_t* pos, uint8_t* kI,
+                          uint8_t* kbar, int64_t n_cap, int32_t* d_status,
+                          void* stream);
+
+/* Recompute every block mean of positions [0, n[b]) from an indexer-K cache
+ * that was filled in place (bulk prefill). n [B] int64 device, each
+ * <= n_max <= n_cap. */
+CSA2_API int csa2_block_means(const uint8_t* kI, int32_t B, int32_t d_I,
+                     const int64_t* n, int64_t n_max, int64_t n_cap,
+                     uint8_t* kbar, int32_t* d_status, void* stream);
+
+/* Append one bf16 sliding-window row per sequence into the layer's ring:
+ * slot = pos[b] mod W [CED].
+ *   x [B][d] bf16; pos [B] int64 device; swa [B][W][d] bf16 */
+CSA2_API int csa2_append_swa(const void* x, int32_t B, int32_t d, const int64_t* pos,
+                    void* swa, int32_t W, void* stream);
+
+/* ---- a3: indexer scores [CSA2] ------------------------------------------ */
+/* Raw indexer scan: scores[b][t] = sum_h w[b][h] * relu(qI[b][h] . kI[b][t])
+ * for t < n[b], FP8 x FP8 products accumulated in fp32 on the tensor cores
+ * (one indexer key per position shared by all heads; no 1/sqrt(d_I)).
+ *   qI [B][H_I][d_I] u8 (E4M3); w [B][H_I] fp32
+ *   kI row (b,t) at kI + (b*kI_seq_stride + t)*d_I (stride 0 = one shared cache)
+ *   n [B] int64 device, every n[b] <= n_max (else CSA2_ERR_DEVICE_BOUNDS)
+ *   scores [B][scores_stride] fp32 */
+CSA2_API int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI,
+                      int64_t kI_seq_stride, const int64_t* n, int32_t B,
+                      int32_t H_I, int32_t d_I, int64_t n_max, float* scores,
+                      int64_t scores_stride, int32_t* d_status, void* stream);
+
+/* ---- a6: Top-K [CSA2] --------------------------------------------------- */
+/* Select, per row b, the k best of its first n[b] candidates by (score
+ * descending, position ascending); write their positions sorted ascending
+ * to idx_out[b][0..k), padded with -1 when fewer than k candidates exist.
+ *   scores [B][scores_stride] fp32 (not NaN)
+ *   cand_pos [B][scores_stride] int32 or NULL: candidate i of row b has
+ *            position cand_pos[b][i] (-1 = absent); NULL means position i.
+ *   n        [B] int64 device, or NULL: every row has n_max candidates.
+ *   k <= 2048. Workspace: CSA2_OP_TOPK. */
+CSA2_API int csa2_topk(const float* scores, const int32_t* cand_pos,
+              int64_t scores_stride, const int64_t* n, int32_t B,
+              int64_t n_max, int32_t k, int32_t* idx_out, void* ws,
+              size_t ws_bytes, void* stream);
+
+/* ---- a3+a6: Full layer indexer [CSA2] ----------------------------------- */
+/* Full mode: score every visible position t < n[b] (csa2_index_scores) and
+ * select a new Top-k (csa2_topk), with the Top-K histogram fused into the
+ * scan. scores_out (NULL allowed) receives the scores [B][n_max].
+ * Workspace: CSA2_OP_INDEX_FULL. */
+CSA2_API int csa2_index_full(const uint8_t* qI, const float* w, const uint8_t* kI,
+                    int64_t kI_seq_stride, const int64_t* n, int32_t B,
+                    int32_t H_I, int32_t d_I, int64_t n_max, int32_t k,
+                    int32_t* idx_out, float* scores_out, void* ws,
+                    size_t ws_bytes, int32_t* d_status, void* stream);
+
+/* ---- a4: hierarchical pool [CSA2] --------------------------------------- */
+/* The Full layer forms a bounded candidate pool: every block of 8 positions
+ * is scored on its mean key (kbar) with the pool-forming indexer query, and
+ * the best min(P, ceil(n/8)) blocks (score desc, block id asc) are written
+ * to pool_out[b][0..P) sorted ascending, -1 padded. P <= 2048.
+ *   kbar row (b,j) at kbar + (b*kbar_seq_stride + j)*d_I
+ * Workspace: CSA2_OP_FORM_POOL (with n_max = positions, not blocks). */
+CSA2_API int csa2_form_pool(const uint8_t* qI, const float* w, const uint8_t* kbar,
+                   int64_t kbar_seq_stride, const int64_t* n, int32_t B,
+                   int32_t H_I, int32_t d_I, int64_t n_max, int32_t P,
+                   int32_t* pool_out, void* ws, size_t ws_bytes,
+                   int32_t* d_status, void* stream);
+
+/* ---- a5+a6: Reindex layer [CSA2] ---------------------------------------- */
+/* Reindex mode: rescore only the positions of the pool's blocks (pool
+ * [B][P] ascending block ids, -1 = empty; positions >= n[b] are absent)
+ * with this layer's own indexer query, then select Top-k over them.
+ * Workspace: CSA2_OP_INDEX_REINDEX. */
+CSA2_API int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t* kI,
+                       int64_t kI_seq_stride, const int64_t* n,
+                       const int32_t* pool, int32_t P, int32_t B, int32_t H_I,
+                       int32_t d_I, int32_t k, int32_t* idx_out, void* ws,
+                       size_t ws_bytes, int32_t* d_status, void* stream);
+
+/* ---- a7+a8+a9: sparse attention over FP4 rows + SWA [CSA2][CED][FP4] --- */
+/* out[b][h] = softmax(scale * q[b][h] . X^T) X over the keys X = the
+ * dequantised main-KV rows idx[b][0..k) (-1 = absent; main K = V) followed
+ * by the first swa_len[b] rows of the sequence's SWA block (K = V, bf16).
+ * Dequantisation (E2M1 x E4M3) is exact in bf16; Q.K^T and P.V run on the
+ * tensor cores in bf16 with fp32 accumulation; the sparse and SWA parts are
+ * computed as split-K partials and merged by log-sum-exp. A row with no key
+ * at all gets zeros.
+ *   q, out   [B][H][d] bf16
+ *   codes/scales row (b,t) at (b*kv_seq_stride + t); t must be < n_cap
+ *            (checked: CSA2_ERR_DEVICE_BOUNDS, key skipped)
+ *   idx      [B][k] int32
+ *   swa      rows of sequence b start at swa + b*swa_seq_stride*d (W = 128
+ *            for decode rings; prefill passes stride 1 so query b's window
+ *            is rows b .. b+swa_len[b]-1 of the chunk's SWA array)
+ *   swa_len  [B] int32 device, each <= W
+ * Workspace: CSA2_OP_SPARSE_ATTN. */
+CSA2_API int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d,
+                     const uint8_t* codes, const uint8_t* scales,
+                     int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx,
+                     int32_t k, const void* swa, int64_t swa_seq_stride,
+                     int32_t W, const int32_t* swa_len, float softmax_scale,
+                     void* out, void* ws, size_t ws_bytes, int32_t* d_status,
+                     void* stream);
+
+/* ---- a10+a11: one layer group [CSA2][TG] -------------------------------- */
+enum csa2_mode { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1 };
+
+/* Arguments of csa2_layer_group. Pointers are device pointers unless noted. */
+typedef struct csa2_group_args {
+  int32_t mode;          /* CSA2_MODE_FULL or CSA2_MODE_REINDEX               */
+  int32_t n_reuse;       /* Reuse layers that follow the first layer          */
+  int32_t form_pool;     /* Full only: also form the pool for later groups    */
+  int32_t B, H, d, H_I, d_I, k, W, P;
+  int64_t n_max;         /* host bound on every n[b]                          */
+  int64_t n_cap;         /* cache capacity (rows per sequence)                */
+  const int64_t* n;      /* [B] visible positions                             */
+  const uint8_t* codes;  /* [B][n_cap][d/2]                                   */
+  const uint8_t* scales; /* [B][n_cap][d/16]                                  */
+  const uint8_t* kI;     /* [B][n_cap][d_I]                                   */
+  const uint8_t* kbar;   /* [B][ceil(n_cap/8)][d_I] (form_pool only)          */
+  const uint8_t* qI;     /* [B][H_I][d_I] the first layer's indexer query     */
+  const float* w;        /* [B][H_I]                                          */
+  const uint8_t* qI_pool;/* pool-forming query (NULL = qI)                    */
+  const float* w_pool;   /* (NULL = w)                                        */
+  int32_t* pool;         /* [B][P]: written if form_pool, read if REINDEX     */
+  int32_t* idx;          /* [B][k]: the group's Top-K (written)               */
+  const void* const* q_layers;    /* HOST array [1+n_reuse] of [B][H][d] bf16 */
+  const void* const* swa_layers;  /* HOST array [1+n_reuse] of [B][W][d] bf16 */
+  const int32_t* swa_len;         /* [B]                                      */
+  void* const* out_layers;        /* HOST array [1+n_reuse] of [B][H][d] bf16 */
+  float softmax_scale;
+  void* ws;              /* workspace, CSA2_OP_LAYER_GROUP                    */
+  size_t ws_bytes;
+  int32_t* d_status;     /* optional                                          */
+  void* const* events;   /* optional HOST array of cudaEvent_t recorded on
+                            the stream: [0] the indexer scan begins, [1] the
+                            scan ends, [2] Top-K (and pool) done, [3 + l]
+                            layer l's attention done                         */
+  int32_t n_events;      /* length of `events` (0 = none)                     */
+} csa2_group_args;
+
+/* Run one CSA2 layer group: the first layer (Full: scan all positions,
+ * Top-K, optionally form the pool; Reindex: rescore the pool, Top-K), then
+ * attention for the first layer and each Reuse layer with the group's
+ * Top-K, each with its own main Q and SWA KV. */
+CSA2_API int csa2_layer_group(const csa2_group_args* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H_ */

@@ -1,0 +1,62 @@
+"""Shared helpers of the GPU parity tests (conversions and comparison rules)."""
+import numpy as np
+import torch
+
+TOPK_BAND = 1e-5          # relative tie band around the oracle's k-th score
+ATTN_MAX_ABS = 2e-3       # bf16 attention output vs float64 oracle
+ATTN_MEAN_ABS = 2e-4
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 bit patterns (numpy, CPU)."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().numpy()
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def check_topk(gpu_idx, oracle_idx, oracle_scores, oracle_pos, k, band=TOPK_BAND):
+    """Top-K parity: sorted ascending, -1 padded, equal sizes, equal sets except
+    for positions whose oracle score lies within `band` (relative) of the
+    oracle's k-th score."""
+    g = np.asarray(gpu_idx, dtype=np.int64)
+    o = np.asarray(oracle_idx, dtype=np.int64)
+    gv, ov = g[g >= 0], o[o >= 0]
+    assert np.all(g[len(gv):] == -1), "GPU index list is not -1 padded at the end"
+    assert np.all(np.diff(gv) > 0), "GPU index list is not strictly ascending"
+    assert len(gv) == len(ov), (len(gv), len(ov))
+    diff = set(gv.tolist()) ^ set(ov.tolist())
+    if not diff:
+        return 0
+    s_of = dict(zip(np.asarray(oracle_pos).tolist(), np.asarray(oracle_scores).tolist()))
+    sk = np.sort(np.asarray([s_of[p] for p in ov.tolist()]))[0] if len(ov) >= k else None
+    assert sk is not None, f"sets differ with fewer than k candidates: {sorted(diff)[:10]}"
+    for p in diff:
+        assert p in s_of, f"GPU picked a position that is not a candidate: {p}"
+        assert abs(s_of[p] - sk) <= band * abs(sk), (p, s_of[p], sk)
+    return len(diff)
+
+
+# With few keys the softmax output grows to O(1), where bf16's own rounding
+# (half-ulp = 2^-9 relative) and bf16 probabilities (2^-9 relative each)
+# exceed the absolute bounds above, which assume hundreds of keys (|o| ~ 0.07).
+# Tests with few keys add this relative term.
+BF16_REL = 2.0 ** -8
+
+
+def check_attn(gpu_out, oracle_out, max_abs=ATTN_MAX_ABS, mean_abs=ATTN_MEAN_ABS, rel=0.0):
+    g = bf16_to_f64(gpu_out)
+    r = np.asarray(oracle_out)
+    d = np.abs(g - r)
+    assert np.all(np.isfinite(g))
+    bound = max_abs + rel * np.abs(r)
+    worst = np.argmax(d - bound)
+    assert np.all(d <= bound), f"abs err {d.flat[worst]:.3e} > bound {bound.flat[worst]:.3e} (max err {d.max():.3e})"
+    mbound = mean_abs + rel * np.abs(r).mean()
+    assert d.mean() <= mbound, f"mean abs err {d.mean():.3e} > {mbound:.3e}"
+    return float(d.max()), float(d.mean())

@@ -1,0 +1,109 @@
+"""GPU parity of the sparse attention (gathered FP4 rows + SWA rows, split-K
+with log-sum-exp merge) against the float64 oracle: max-abs <= 2e-3 and
+mean-abs <= 2e-4 on the bf16 output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from fp4_kv_cache_06_b300 import csa2
+from tests._parity import BF16_REL, bits16, check_attn, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _cache(B, n_cap, seed):
+    kv = synth.normal_bf16((B, n_cap, 512), seed=seed, stream="kv").to(DEV)
+    codes = torch.empty((B, n_cap, 256), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((B, n_cap, 32), dtype=torch.uint8, device=DEV)
+    csa2.csa2_quantize_kv_fp4(kv, codes, scales)
+    return kv, codes, scales
+
+
+def _oracle_cache(kv_cpu_bits):
+    return oracle.quantize_fp4(kv_cpu_bits)
+
+
+@pytest.mark.parametrize("B,H,k,n", [(1, 16, 512, 2048), (3, 64, 512, 3000), (2, 64, 512, 400), (5, 32, 256, 1000), (8, 48, 64, 100)])
+def test_sparse_attn_matches_oracle(B, H, k, n):
+    W = 128
+    kv, codes, scales = _cache(B, n, seed=B * 100 + H)
+    rng = np.random.default_rng(B + H)
+    idx = np.full((B, k), -1, dtype=np.int32)
+    for b in range(B):
+        m = min(k, n) if b % 2 == 0 else min(k, n) // 2       # some rows partly absent
+        idx[b, :m] = np.sort(rng.permutation(n)[:m])
+    swa_len = np.array([W if b % 3 != 1 else 17 for b in range(B)], dtype=np.int32)
+    q = synth.normal_bf16((B, H, 512), seed=7, stream="q").to(DEV)
+    swa = synth.normal_bf16((B, W, 512), seed=7, stream="swa").to(DEV)
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa,
+                          torch.from_numpy(swa_len).to(DEV), out, ws)
+    torch.cuda.synchronize()
+    kvb, qb, swab = bits16(kv), bits16(q), bits16(swa)
+    ref = np.zeros((B, H, 512))
+    for b in range(B):
+        c, s = oracle.quantize_fp4(kvb[b])
+        np.testing.assert_array_equal(u8(codes)[b], c)
+        ref[b] = oracle.sparse_attention(qb[b], c, s, idx[b], swab[b], swa_len[b])
+    few_keys = (idx >= 0).sum(1).min() + swa_len.min() < 300
+    check_attn(out, ref, rel=BF16_REL if few_keys else 0.0)
+
+
+def test_sparse_attn_empty_and_swa_only():
+    B, H, k, n, W = 2, 64, 512, 100, 128
+    kv, codes, scales = _cache(B, n, seed=9)
+    idx = torch.full((B, k), -1, dtype=torch.int32, device=DEV)
+    swa_len = torch.tensor([0, 5], dtype=torch.int32, device=DEV)
+    q = synth.normal_bf16((B, H, 512), seed=9, stream="q").to(DEV)
+    swa = synth.normal_bf16((B, W, 512), seed=9, stream="swa").to(DEV)
+    out = torch.full((B, H, 512), 7.0, dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, idx, swa, swa_len, out, ws)
+    torch.cuda.synchronize()
+    assert torch.all(out[0] == 0)
+    ref = oracle.sparse_attention(bits16(q)[1], np.zeros((0, 256), np.uint8), np.zeros((0, 32), np.uint8),
+                                  np.full(k, -1), bits16(swa)[1], 5)
+    check_attn(out[1:], ref[None], rel=BF16_REL)
+
+
+def test_sparse_attn_out_of_range_index_is_reported_and_skipped():
+    B, H, k, n, W = 1, 16, 64, 50, 128
+    kv, codes, scales = _cache(B, n, seed=4)
+    idxn = np.arange(k, dtype=np.int32)[None]              # 50..63 are >= n_cap
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q = synth.normal_bf16((B, H, 512), seed=4, stream="q").to(DEV)
+    swa = synth.normal_bf16((B, W, 512), seed=4, stream="swa").to(DEV)
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idxn).to(DEV), swa,
+                          torch.tensor([W], dtype=torch.int32, device=DEV), out, ws, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 6
+    c, s = oracle.quantize_fp4(bits16(kv)[0])
+    ref = oracle.sparse_attention(bits16(q)[0], c, s, np.where(idxn[0] < n, idxn[0], -1), bits16(swa)[0], W)
+    check_attn(out, ref[None], rel=BF16_REL)
+
+
+def test_prefill_layout_shared_cache_and_sliding_rows():
+    """Prefill form: every query reads one shared cache (stride 0) and its own
+    window of a chunk's SWA rows (stride 1 row)."""
+    Q, H, k, n, W = 40, 64, 512, 1500, 128
+    kv, codes, scales = _cache(1, n, seed=12)
+    rng = np.random.default_rng(12)
+    idx = np.stack([np.sort(rng.permutation(n)[:k]) for _ in range(Q)]).astype(np.int32)
+    q = synth.normal_bf16((Q, H, 512), seed=12, stream="q").to(DEV)
+    swa_rows = synth.normal_bf16((Q + W - 1, 512), seed=12, stream="swa").to(DEV)
+    swa_len = torch.full((Q,), W, dtype=torch.int32, device=DEV)
+    out = torch.empty((Q, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, Q, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa_rows, swa_len, out, ws,
+                          kv_seq_stride=0, swa_seq_stride=1, W=W)
+    torch.cuda.synchronize()
+    c, s = oracle.quantize_fp4(bits16(kv)[0])
+    sb, qb = bits16(swa_rows), bits16(q)
+    ref = np.stack([oracle.sparse_attention(qb[i], c, s, idx[i], sb[i:i + W], W) for i in range(Q)])
+    check_attn(out, ref)

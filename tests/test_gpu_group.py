@@ -1,0 +1,121 @@
+"""GPU parity of whole CSA2 layer groups through csa2_layer_group: the small
+single-query Full layer (batch 1, 2048 positions, 4x64 indexer, 16 heads) and
+Full+Reuse / pool+Reindex+Reuse groups at reduced sizes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from fp4_kv_cache_06_b300 import csa2
+from tests._parity import bits16, check_attn, check_topk, u8
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _group_inputs(B, n, n_cap, H, H_I, d_I, L, seed, bias=0.0):
+    kv = synth.normal_bf16((B, n_cap, 512), seed=seed, stream="kv").to(DEV)
+    codes = torch.empty((B, n_cap, 256), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((B, n_cap, 32), dtype=torch.uint8, device=DEV)
+    csa2.csa2_quantize_kv_fp4(kv, codes, scales)
+    kI = synth.indexer_keys_e4m3((B, n_cap, d_I), seed=seed, bias_prob=bias).to(DEV)
+    kbar = torch.zeros((B, (n_cap + 7) // 8, d_I), dtype=torch.uint8, device=DEV)
+    nt = torch.full((B,), n, dtype=torch.int64, device=DEV)
+    csa2.csa2_block_means(kI, nt, kbar, n_max=n)
+    qI = synth.normal_e4m3((B, H_I, d_I), seed=seed, stream="qI").to(DEV)
+    w = synth.uniform_f32((B, H_I), seed=seed, stream="w").to(DEV)
+    qs = [synth.normal_bf16((B, H, 512), seed=seed, stream="q", sub=l).to(DEV) for l in range(L)]
+    swas = [synth.normal_bf16((B, 128, 512), seed=seed, stream="swa", sub=l).to(DEV) for l in range(L)]
+    return dict(kv=kv, codes=codes, scales=scales, kI=kI, kbar=kbar, n=nt, qI=qI, w=w, qs=qs, swas=swas)
+
+
+def _run(mode, inp, n, L, k=512, P=2048, form_pool=False, qP=None, wP=None, pool=None):
+    B, H = inp["qs"][0].shape[:2]
+    idx = torch.empty((B, k), dtype=torch.int32, device=DEV)
+    if pool is None:
+        pool = torch.full((B, P), -1, dtype=torch.int32, device=DEV)
+    outs = [torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    swa_len = torch.full((B,), min(n, 128), dtype=torch.int32, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_LAYER_GROUP, B, inp["codes"].shape[1], k, P, H))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa2.csa2_layer_group(mode, inp["n"], inp["codes"].shape[1], inp["codes"], inp["scales"], inp["kI"],
+                          inp["qI"], inp["w"], idx, inp["qs"], inp["swas"], swa_len, outs, ws,
+                          kbar=inp["kbar"], pool=pool, form_pool=form_pool, qI_pool=qP, w_pool=wP, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return idx, pool, outs
+
+
+def _attn_on_oracle_idx(inp, layer, b, ref_idx, c, s):
+    """Attention parity with the oracle's own Top-K fed to the kernel (used
+    when the group's Top-K differs from the oracle's inside the tie band)."""
+    H = inp["qs"][layer].shape[1]
+    out = torch.empty((1, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, 1, 0, 512, 2048, H))
+    q = inp["qs"][layer][b:b + 1].contiguous()
+    swa = inp["swas"][layer][b:b + 1].contiguous()
+    csa2.csa2_sparse_attn(q, inp["codes"][b:b + 1].contiguous(), inp["scales"][b:b + 1].contiguous(),
+                          torch.from_numpy(np.asarray(ref_idx, dtype=np.int32)[None]).to(DEV), swa,
+                          torch.tensor([128], dtype=torch.int32, device=DEV), out, ws)
+    torch.cuda.synchronize()
+    ref = oracle.sparse_attention(bits16(q)[0], c, s, ref_idx, bits16(swa)[0], 128)
+    check_attn(out, ref[None])
+
+
+def _check_layers(inp, outs, b, gpu_idx, ref_idx, c, s):
+    for l in range(len(outs)):
+        if np.array_equal(gpu_idx, ref_idx):
+            ref = oracle.sparse_attention(bits16(inp["qs"][l])[b], c, s, ref_idx, bits16(inp["swas"][l])[b], 128)
+            check_attn(outs[l][b:b + 1], ref[None])
+        else:
+            _attn_on_oracle_idx(inp, l, b, ref_idx, c, s)
+
+
+def test_single_query_full_layer_small_config():
+    """Batch 1, 2048 positions, indexer 4x64, Top-512, 16 heads, SWA 128."""
+    B, n, H = 1, 2048, 16
+    inp = _group_inputs(B, n, n, H, 4, 64, 1, seed=2024)
+    idx, _, outs = _run(csa2.MODE_FULL, inp, n, 1)
+    c, s = oracle.quantize_fp4(bits16(inp["kv"])[0])
+    ref_idx, ref_s = oracle.full_topk(u8(inp["qI"])[0], inp["w"].cpu().numpy()[0], u8(inp["kI"])[0], n)
+    gi = idx.cpu().numpy()[0]
+    check_topk(gi, ref_idx, ref_s, np.arange(n), 512)
+    _check_layers(inp, outs, 0, gi, ref_idx, c, s)
+
+
+def test_full_group_with_reuse_and_pool():
+    B, n, H, L = 3, 20000, 64, 4
+    inp = _group_inputs(B, n, n + 8, H, 8, 128, L, seed=77, bias=0.05)
+    idx, pool, outs = _run(csa2.MODE_FULL, inp, n, L, form_pool=True, P=512)
+    gi, gp = idx.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        c, s = oracle.quantize_fp4(bits16(inp["kv"])[b])
+        ref_idx, ref_s = oracle.full_topk(u8(inp["qI"])[b], inp["w"].cpu().numpy()[b], u8(inp["kI"])[b], n)
+        check_topk(gi[b], ref_idx, ref_s, np.arange(n), 512)
+        kb = oracle.block_means(u8(inp["kI"])[b], n)
+        ref_pool, ref_bs = oracle.form_pool(u8(inp["qI"])[b], inp["w"].cpu().numpy()[b], kb, 512)
+        check_topk(gp[b], ref_pool, ref_bs, np.arange(kb.shape[0]), 512)
+        _check_layers(inp, outs, b, gi[b], ref_idx, c, s)
+    # Reuse: every layer used the group's indices -> recompute on them agrees
+    # (checked above per layer); and different layers give different outputs
+    assert not torch.equal(outs[0], outs[1])
+
+
+def test_reindex_group_with_pool_formation():
+    B, n, H, L, P = 2, 40000, 64, 4, 2048
+    inp = _group_inputs(B, n, n, H, 8, 128, L, seed=88)
+    qP = synth.normal_e4m3((B, 8, 128), seed=88, stream="qI_pool").to(DEV)
+    wP = synth.uniform_f32((B, 8), seed=88, stream="w_pool").to(DEV)
+    idx, pool, outs = _run(csa2.MODE_REINDEX, inp, n, L, form_pool=True, qP=qP, wP=wP, P=P)
+    gi, gp = idx.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        c, s = oracle.quantize_fp4(bits16(inp["kv"])[b])
+        kb = oracle.block_means(u8(inp["kI"])[b], n)
+        ref_pool, ref_bs = oracle.form_pool(u8(qP)[b], wP.cpu().numpy()[b], kb, P)
+        check_topk(gp[b], ref_pool, ref_bs, np.arange(kb.shape[0]), P)
+        if not np.array_equal(gp[b], ref_pool):
+            continue
+        ref_idx, ref_s, ref_pos = oracle.reindex_topk(u8(inp["qI"])[b], inp["w"].cpu().numpy()[b], u8(inp["kI"])[b], ref_pool, n)
+        check_topk(gi[b], ref_idx, ref_s, ref_pos, 512)
+        _check_layers(inp, outs, b, gi[b], ref_idx, c, s)
