@@ -8,7 +8,7 @@ import torch
 import oracle
 import synth
 from fp4_kv_cache_06_b300 import csa2
-from tests._parity import BF16_REL, bits16, check_attn, u8
+from tests._parity import bits16, check_attn, u8, vmax_of
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -45,12 +45,16 @@ def test_sparse_attn_matches_oracle(B, H, k, n):
     torch.cuda.synchronize()
     kvb, qb, swab = bits16(kv), bits16(q), bits16(swa)
     ref = np.zeros((B, H, 512))
+    vmax = np.zeros((B, 1, 512))
     for b in range(B):
         c, s = oracle.quantize_fp4(kvb[b])
         np.testing.assert_array_equal(u8(codes)[b], c)
         ref[b] = oracle.sparse_attention(qb[b], c, s, idx[b], swab[b], swa_len[b])
+        sel = idx[b][idx[b] >= 0]
+        vmax[b, 0] = vmax_of(np.concatenate([oracle.dequant_fp4(c[sel], s[sel]),
+                                             oracle.bf16_bits_to_f64(swab[b][:swa_len[b]])]))
     few_keys = (idx >= 0).sum(1).min() + swa_len.min() < 300
-    check_attn(out, ref, rel=BF16_REL if few_keys else 0.0)
+    check_attn(out, ref, vmax=vmax if few_keys else None)
 
 
 def test_sparse_attn_empty_and_swa_only():
@@ -67,7 +71,7 @@ def test_sparse_attn_empty_and_swa_only():
     assert torch.all(out[0] == 0)
     ref = oracle.sparse_attention(bits16(q)[1], np.zeros((0, 256), np.uint8), np.zeros((0, 32), np.uint8),
                                   np.full(k, -1), bits16(swa)[1], 5)
-    check_attn(out[1:], ref[None], rel=BF16_REL)
+    check_attn(out[1:], ref[None], vmax=vmax_of(oracle.bf16_bits_to_f64(bits16(swa)[1][:5])))
 
 
 def test_sparse_attn_out_of_range_index_is_reported_and_skipped():
@@ -85,7 +89,8 @@ def test_sparse_attn_out_of_range_index_is_reported_and_skipped():
     assert st.item() == 6
     c, s = oracle.quantize_fp4(bits16(kv)[0])
     ref = oracle.sparse_attention(bits16(q)[0], c, s, np.where(idxn[0] < n, idxn[0], -1), bits16(swa)[0], W)
-    check_attn(out, ref[None], rel=BF16_REL)
+    keys = np.concatenate([oracle.dequant_fp4(c, s), oracle.bf16_bits_to_f64(bits16(swa)[0])])
+    check_attn(out, ref[None], vmax=vmax_of(keys))
 
 
 def test_prefill_layout_shared_cache_and_sliding_rows():
