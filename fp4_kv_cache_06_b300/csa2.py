@@ -335,3 +335,25 @@ def csa2_layer_group(mode, n, n_max, codes, scales, kI, qI, w, idx, q_layers: Se
         a.events, a.n_events = None, 0
     rc = lib().csa2_layer_group(ctypes.byref(a), _stream(stream))
     _check(rc, "csa2_layer_group")
+
+
+def csa2_topk_noalloc(scores, n, n_max, k, idx_out, cand_pos=None, stream=None):
+    """Top-K like csa2_topk but with no workspace argument.
+
+    For callers that cannot allocate device memory: the library keeps the
+    scratch in a fixed per-GPU device array (at most 64 rows per call).
+    Calls that overlap on the GPU share that array and race; keep them
+    ordered on one stream. The first call on a device does a one-time
+    lookup of the array's address, so make it before any stream capture.
+    """
+    L = lib()
+    f = L.csa2_topk_noalloc
+    f.restype = ctypes.c_int
+    f.argtypes = [_c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i32, _c_p, _c_p]
+    _need(scores, "scores", torch.float32, 2)
+    _opt(n, "n", torch.int64, 1)
+    _need(idx_out, "idx_out", torch.int32, 2)
+    _opt(cand_pos, "cand_pos", torch.int32, 2)
+    rc = f(_ptr(scores), _ptr(cand_pos), scores.shape[1], _ptr(n), scores.shape[0], int(n_max), int(k),
+           _ptr(idx_out), _stream(stream))
+    _check(rc, "csa2_topk_noalloc")

@@ -163,6 +163,30 @@ CSA2_API int csa2_topk(const float* scores, const int32_t* cand_pos,
               int64_t n_max, int32_t k, int32_t* idx_out, void* ws,
               size_t ws_bytes, void* stream);
 
+/* ---- Top-K without a caller workspace ----------------------------------- */
+/* The source pages have no counterpart to this call; it exists for callers
+ * of this library that cannot allocate device memory: code running inside
+ * another runtime's execution hook where allocation is forbidden (an
+ * inference-engine plugin's enqueue, say), steady-state serving loops that
+ * must never call cudaMalloc because it can synchronise the whole device,
+ * and plain C callers with no allocator of their own.
+ * Same selection, arguments and result as csa2_topk, minus the workspace:
+ * the scratch lives in a fixed device array inside the library, reserved on
+ * every GPU that loads the library and held until the process exits
+ * (about 5.25 MB). Limits: at most CSA2_TOPK_NOALLOC_MAX_ROWS rows (B);
+ * larger B returns CSA2_ERR_UNSUPPORTED_SHAPE and enqueues nothing.
+ * The first call made while a device is current looks up that device's
+ * array address (one-time set-up); make that first call before capturing
+ * any stream. All calls share the one array and each call re-zeroes what
+ * must start at zero, so calls whose GPU work overlaps (different streams,
+ * or unordered host threads) race and return wrong results: order them on
+ * one stream. Calls no cudaMalloc/cudaFree or allocating routine. */
+#define CSA2_TOPK_NOALLOC_MAX_ROWS 64
+CSA2_API int csa2_topk_noalloc(const float* scores, const int32_t* cand_pos,
+                               int64_t scores_stride, const int64_t* n,
+                               int32_t B, int64_t n_max, int32_t k,
+                               int32_t* idx_out, void* stream);
+
 /* ---- a3+a6: Full layer indexer [CSA2] ----------------------------------- */
 /* Full mode: score every visible position t < n[b] (csa2_index_scores) and
  * select a new Top-k (csa2_topk), with the Top-K histogram fused into the
