@@ -84,58 +84,73 @@ def max_over_ranks(x, world, device):
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
+_POLLER = r"""
+import sys, time
+import pynvml
+pynvml.nvmlInit()
+uuid = sys.argv[1]
+try:
+    h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+except Exception:
+    h = pynvml.nvmlDeviceGetHandleByIndex(int(sys.argv[2]))
+print("max", pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM), flush=True)
+while True:
+    sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
+    r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
+    print(sm, r, flush=True)
+    time.sleep(0.002)
+"""
+
+
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock-event (throttle) reasons of one GPU
+    every ~2 ms from a separate process while the timed region runs
+    (read-only NVML queries; no GPU setting is changed)."""
+    HW_SLOWDOWN, SW_POWER_CAP, SW_THERMAL, HW_THERMAL = 0x8, 0x4, 0x20, 0x40
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.out = ""
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
+            import torch
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.gpu).uuid)
+            self.proc = subprocess.Popen([sys.executable, "-c", _POLLER, uuid, str(self.gpu)],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)                      # let the poller start before the timed region
         except Exception:
             self.proc = None
         return self
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
 
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self.out, _ = self.proc.communicate(timeout=5)
             except Exception:
                 self.proc.kill()
-            self.thread.join(timeout=2)
+                self.out = ""
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
+        sm_max, samples = None, []
+        for ln in self.out.splitlines():
+            parts = ln.split()
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+                if parts[0] == "max":
+                    sm_max = float(parts[1])
+                else:
+                    samples.append((float(parts[0]), int(parts[1])))
+            except (ValueError, IndexError):
+                pass
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": sm_max, "reasons": ["unavailable"], "samples": 0}
+        names = {self.HW_SLOWDOWN: "hw_slowdown", self.HW_THERMAL: "hw_thermal_slowdown",
+                 self.SW_THERMAL: "sw_thermal_slowdown", self.SW_POWER_CAP: "sw_power_cap"}
+        seen = {nm for _, r in samples for bit, nm in names.items() if r & bit}
+        return {"sm_mhz": statistics.median(x for x, _ in samples), "sm_max_mhz": sm_max,
+                "reasons": sorted(seen), "samples": len(samples)}
 
 
 # ---------------------------------------------------------------------------
@@ -183,8 +198,8 @@ class DecodeWorkload:
         self.w = [synth.uniform_f32((B, H_I), seed, "w", dev, sub=g) for g in range(G)]
         self.qI_pool = synth.normal_e4m3((B, H_I, d_I), seed, "qI_pool", dev)
         self.w_pool = synth.uniform_f32((B, H_I), seed, "w_pool", dev)
-        self.kv_new = synth.normal_bf16((B, 1, 512), seed, "kv_new", dev)
-        self.kI_new = synth.indexer_keys_e4m3((B, 1, d_I), seed + 1, dev, bias_prob=cfg.bias_prob)
+        self.kv_new = synth.normal_bf16((B, 512), seed, "kv_new", dev)
+        self.kI_new = synth.indexer_keys_e4m3((B, d_I), seed + 1, dev, bias_prob=cfg.bias_prob)
         self.swa_new = [synth.normal_bf16((B, 512), seed, "swa_new", dev, sub=l) for l in range(self.layers)]
         self.idx = [torch.empty((B, k), dtype=i32, device=dev) for _ in range(G)]
         self.pool = torch.full((B, P), -1, dtype=i32, device=dev)
@@ -207,10 +222,8 @@ class DecodeWorkload:
         if self.step_i > 0 and self.cfg.steps > 1:
             self.pos.add_(1)
             self.n.add_(1)
-        csa2.csa2_quantize_kv_fp4(self.kv_new, self.codes, self.scales, pos=self.pos)
-        csa2.csa2_append_indexer_k(self.kI_new, self.kI, self.kbar, pos=self.pos)
-        for l in range(self.layers):
-            csa2.csa2_append_swa(self.swa_new[l], self.pos, self.swa[l])
+        csa2.csa2_append_step(self.kv_new, self.kI_new, self.swa_new, self.swa, self.pos, self.codes,
+                              self.scales, self.kI, self.kbar)
         n_max = self.n_first + (self.cfg.steps - 1 if self.cfg.steps > 1 else 0)
         n_max = min(n_max, self.n_cap)
         l0 = 0
@@ -260,6 +273,122 @@ class DecodeWorkload:
         self.step()
         for d, s in zip(self.h_out, self.out):
             d.copy_(s, non_blocking=True)
+
+
+class PrefillWorkload:
+    """One encoder prefill chunk: queries at tokens p0..p0+Q-1 over a shared FP4
+    cache of n compressed entries (ratio 2), Full + Reuse layers."""
+
+    def __init__(self, cfg, device, seed=1234, queries=None):
+        import torch
+        import synth
+        from fp4_kv_cache_06_b300 import csa2
+        self.torch, self.csa2, self.cfg, self.dev = torch, csa2, cfg, device
+        Q = self.Q = queries or cfg.prefill_queries
+        n, H, W, k = cfg.n, cfg.H, cfg.W, cfg.k
+        self.n_keys = n
+        tokens = n * cfg.ratio                               # context incl. the chunk
+        self.p0 = tokens - Q
+        dev = device
+        self.codes = torch.empty((n, 256), dtype=torch.uint8, device=dev)
+        self.scales = torch.empty((n, 32), dtype=torch.uint8, device=dev)
+        chunk = 1 << 16
+        for c0 in range(0, n, chunk):
+            r = min(chunk, n - c0)
+            x = synth.normal_bf16((1, r, 512), seed, "kv", dev, sub=c0 // chunk)
+            csa2.csa2_quantize_kv_fp4(x, self.codes[None], self.scales[None],
+                                      pos=torch.tensor([c0], dtype=torch.int64, device=dev))
+        self.kI = synth.indexer_keys_e4m3((n, cfg.d_I), seed, dev)
+        self.qI = synth.normal_e4m3((Q, cfg.H_I, cfg.d_I), seed, "qI", dev)
+        self.w = synth.uniform_f32((Q, cfg.H_I), seed, "w", dev)
+        self.layers = 1 + cfg.groups[0][1]
+        self.q = [synth.normal_bf16((Q, H, 512), seed, "q", dev, sub=l) for l in range(self.layers)]
+        self.swa = [synth.normal_bf16((Q + W - 1, 512), seed, "swa", dev, sub=l) for l in range(self.layers)]
+        self.out = [torch.empty((Q, H, 512), dtype=torch.bfloat16, device=dev) for _ in range(self.layers)]
+        pos = torch.arange(self.p0, self.p0 + Q, device=dev, dtype=torch.int64)
+        self.n_vis = torch.clamp((pos + 1) // cfg.ratio, max=n).contiguous()
+        self.swa_len = torch.clamp(pos + 1, max=W).to(torch.int32).contiguous()
+        self.idx = torch.empty((Q, k), dtype=torch.int32, device=dev)
+        self.ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_PREFILL_GROUP, Q, n, k, 0, H), dev)
+        self.B = Q
+        torch.cuda.synchronize()
+
+    def step(self, events=None):
+        self.csa2.csa2_prefill_group(self.n_vis, self.codes, self.scales, self.kI, self.qI, self.w, self.idx,
+                                     self.q, self.swa, self.swa_len, self.out, self.ws, events=events)
+
+    def gemm_flops(self):
+        return 2.0 * self.Q * self.cfg.H_I * self.n_keys * self.cfg.d_I
+
+    def attn_flops_per_layer(self):
+        return 4.0 * self.Q * self.cfg.H * (self.cfg.k + self.cfg.W) * 512
+
+
+def run_prefill(args, world, rank, local):
+    import torch
+    import synth
+    from fp4_kv_cache_06_b300 import csa2
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.get_config(args.config)
+    wl = PrefillWorkload(cfg, dev, seed=1234 + 7919 * rank, queries=args.batch)
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+
+    def mk():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+    nev = 3 + wl.layers
+    evs = [[mk() for _ in range(nev)] for _ in range(args.steps)]
+    step_ev = [(mk(), mk()) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    launches0 = csa2.launch_count()
+    barrier(world)
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            step_ev[i][0].record()
+            wl.step(events=evs[i])
+            step_ev[i][1].record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    launches = csa2.launch_count() - launches0
+    ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
+    ms_max = max_over_ranks(ms, world, dev)
+    gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    attn_ms = statistics.mean(e[2 + j].elapsed_time(e[3 + j]) for e in evs for j in range(wl.layers))
+    bf16 = 1765.8
+    try:
+        with open(PEAKS_FILE) as f:
+            bf16 = float(json.load(f)["bf16_tflops"])
+        kind = "measured bf16 x 2 (nominal fp8/bf16 ratio)"
+    except Exception:
+        bf16, kind = 1800.0, "fallback bf16 x 2"
+    fp8_peak = 2 * bf16
+    ach = wl.gemm_flops() / (gemm_ms / 1e3) / 1e12
+    res = {
+        "metric": "CSA2 prefill query tokens/s per encoder group (ratio 2); % of B300 FP8 tensor roofline",
+        "value": world * wl.Q / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
+        "config": {"workload": cfg.workload, "config_index": args.config, "queries": wl.Q, "entries": wl.n_keys,
+                   "first_query_token": wl.p0, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}",
+                   "topk": cfg.k, "swa": cfg.W, "layers": wl.layers, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (2 GiB score matrix per step)"},
+        "roofline": {"bound": "tensor", "kernel": "k_prefill_index (tcgen05 FP8 indexer GEMM)",
+                     "achieved": round(ach, 1), "peak": fp8_peak, "peak_kind": kind, "unit": "TFLOP/s",
+                     "frac": round(ach / fp8_peak, 4), "traffic": None, "gemm_ms": round(gemm_ms, 4),
+                     "algorithmic_flops_per_launch": wl.gemm_flops()},
+        "gpu_launches": int(launches), "clocks": clk.summary(),
+        "phases_ms": {"indexer_gemm_ms": gemm_ms, "topk_ms": topk_ms, "attn_ms_per_layer": attn_ms,
+                      "attn_tflops": wl.attn_flops_per_layer() / (attn_ms / 1e3) / 1e12},
+        "wall_s": wall,
+    }
+    return res
 
 
 def source_hash(path):
@@ -496,7 +625,7 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
@@ -512,9 +641,13 @@ def main():
             print(json.dumps(run_reference(args, world, 0)), flush=True)
         return
     world, rank, local = dist_setup(args.gpus)
-    res = run_csa2(args, world, rank, local)
+    import synth
+    if synth.get_config(args.config).prefill_queries:
+        res = run_prefill(args, world, rank, local)
+    else:
+        res = run_csa2(args, world, rank, local)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and not synth.get_config(args.config).prefill_queries:
             import synth
             dt, desc = oracle_baseline(synth.get_config(args.config))
             res["cpu_baseline"] = {"value": 1.0 / dt, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",

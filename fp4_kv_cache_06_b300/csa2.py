@@ -18,13 +18,15 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 
 OK = 0
 OP_TOPK, OP_INDEX_FULL, OP_INDEX_REINDEX, OP_FORM_POOL, OP_SPARSE_ATTN, OP_LAYER_GROUP = 1, 2, 3, 4, 5, 6
+OP_PREFILL_GROUP = 7
 MODE_FULL, MODE_REINDEX = 0, 1
 
 EXPORTS = (
     "csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size",
     "csa2_quantize_kv_fp4", "csa2_append_indexer_k", "csa2_block_means", "csa2_append_swa",
     "csa2_index_scores", "csa2_topk", "csa2_index_full", "csa2_form_pool", "csa2_index_reindex",
-    "csa2_sparse_attn", "csa2_layer_group",
+    "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_prefill_index_scores",
+    "csa2_prefill_group",
 )
 
 _c_p, _c_i32, _c_i64, _c_sz, _c_f = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -48,6 +50,18 @@ class GroupArgs(ctypes.Structure):
         ("swa_len", _c_p), ("out_layers", ctypes.POINTER(_c_p)),
         ("softmax_scale", _c_f), ("ws", _c_p), ("ws_bytes", _c_sz), ("d_status", _c_p),
         ("events", ctypes.POINTER(_c_p)), ("n_events", _c_i32),
+    ]
+
+
+class PrefillArgs(ctypes.Structure):
+    """Mirror of ``csa2_prefill_args`` (include/csa2.h)."""
+    _fields_ = [
+        ("Q", _c_i32), ("n_reuse", _c_i32), ("H", _c_i32), ("d", _c_i32), ("H_I", _c_i32), ("d_I", _c_i32),
+        ("k", _c_i32), ("W", _c_i32), ("n_keys", _c_i64), ("n_vis", _c_p),
+        ("codes", _c_p), ("scales", _c_p), ("kI", _c_p), ("qI", _c_p), ("w", _c_p), ("idx", _c_p),
+        ("q_layers", ctypes.POINTER(_c_p)), ("swa_layers", ctypes.POINTER(_c_p)), ("swa_len", _c_p),
+        ("out_layers", ctypes.POINTER(_c_p)), ("softmax_scale", _c_f), ("ws", _c_p), ("ws_bytes", _c_sz),
+        ("d_status", _c_p), ("events", ctypes.POINTER(_c_p)), ("n_events", _c_i32),
     ]
 
 
@@ -77,8 +91,12 @@ def lib() -> ctypes.CDLL:
     L.csa2_index_full.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]
     L.csa2_form_pool.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_p, _c_p, _c_sz, _c_p, _c_p]
     L.csa2_index_reindex.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_sz, _c_p, _c_p]
-    L.csa2_sparse_attn.argtypes = [_c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_i32, _c_p, _c_f, _c_p, _c_p, _c_sz, _c_p, _c_p]
+    L.csa2_sparse_attn.argtypes = [_c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_i32, _c_i32, _c_p, _c_f, _c_p, _c_p, _c_sz, _c_p, _c_p]
     L.csa2_layer_group.argtypes = [ctypes.POINTER(GroupArgs), _c_p]
+    L.csa2_prefill_index_scores.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p]
+    L.csa2_prefill_group.argtypes = [ctypes.POINTER(PrefillArgs), _c_p]
+    L.csa2_append_step.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32,
+                                   _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p]
     for name in EXPORTS:
         if name not in ("csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size"):
             getattr(L, name).restype = ctypes.c_int
@@ -184,6 +202,33 @@ def csa2_append_swa(x, pos, swa, stream=None):
     _check(rc, "csa2_append_swa")
 
 
+def csa2_append_step(kv_new, kI_new, swa_new: Sequence[torch.Tensor], swa: Sequence[torch.Tensor], pos, codes,
+                     scales, kI, kbar=None, d_status=None, stream=None):
+    """One decode token into every cache in one launch: kv_new [B][512] bf16 (FP4 main KV),
+    kI_new [B][d_I] u8 (indexer key + block mean), swa_new[l] [B][512] -> swa[l] [B][W][512]."""
+    _need(kv_new, "kv_new", torch.bfloat16, 2)
+    _need(kI_new, "kI_new", torch.uint8, 2)
+    _need(pos, "pos", torch.int64, 1)
+    _need(codes, "codes", torch.uint8, 3)
+    _need(scales, "scales", torch.uint8, 3)
+    _need(kI, "kI", torch.uint8, 3)
+    _opt(kbar, "kbar", torch.uint8, 3)
+    L = len(swa_new)
+    if len(swa) != L:
+        raise ValueError("swa_new and swa must have the same length")
+    for i in range(L):
+        _need(swa_new[i], f"swa_new[{i}]", torch.bfloat16, 2)
+        _need(swa[i], f"swa[{i}]", torch.bfloat16, 3)
+    B, d = kv_new.shape
+    W = swa[0].shape[1] if L else 1
+    sn = (_c_p * max(L, 1))(*[t.data_ptr() for t in swa_new])
+    sw = (_c_p * max(L, 1))(*[t.data_ptr() for t in swa])
+    rc = lib().csa2_append_step(_ptr(kv_new), _ptr(kI_new), sn, sw, L, W, B, d, kI_new.shape[1], _ptr(pos),
+                                _ptr(codes), _ptr(scales), _ptr(kI), _ptr(kbar), codes.shape[1], _ptr(d_status),
+                                _stream(stream))
+    _check(rc, "csa2_append_step")
+
+
 def csa2_index_scores(qI, w, kI, n, n_max, scores, kI_seq_stride=None, d_status=None, stream=None):
     """scores[b][t] = sum_h w[b][h] relu(qI[b][h] . kI[b][t]) for t < n[b]."""
     _need(qI, "qI", torch.uint8, 3)
@@ -258,7 +303,7 @@ def csa2_index_reindex(qI, w, kI, n, pool, k, idx_out, ws, kI_seq_stride=None, d
 
 
 def csa2_sparse_attn(q, codes, scales, idx, swa, swa_len, out, ws, softmax_scale=None, kv_seq_stride=None,
-                     swa_seq_stride=None, W=None, d_status=None, stream=None):
+                     swa_seq_stride=None, W=None, swa_tail=False, d_status=None, stream=None):
     """q/out [B][H][512] bf16; codes/scales: [B or 1][n_cap][...]; idx [B][k] i32; swa rows bf16."""
     _need(q, "q", torch.bfloat16, 3)
     _need(codes, "codes", torch.uint8, 3)
@@ -275,7 +320,7 @@ def csa2_sparse_attn(q, codes, scales, idx, swa, swa_len, out, ws, softmax_scale
     sws = Wv if swa_seq_stride is None else int(swa_seq_stride)
     scale = (1.0 / d ** 0.5) if softmax_scale is None else float(softmax_scale)
     rc = lib().csa2_sparse_attn(_ptr(q), B, H, d, _ptr(codes), _ptr(scales), kvs, n_cap, _ptr(idx), idx.shape[1],
-                                _ptr(swa), sws, Wv, _ptr(swa_len), scale, _ptr(out), _ptr(ws), ws.numel(),
+                                _ptr(swa), sws, Wv, int(bool(swa_tail)), _ptr(swa_len), scale, _ptr(out), _ptr(ws), ws.numel(),
                                 _ptr(d_status), _stream(stream))
     _check(rc, "csa2_sparse_attn")
 
@@ -335,6 +380,60 @@ def csa2_layer_group(mode, n, n_max, codes, scales, kI, qI, w, idx, q_layers: Se
         a.events, a.n_events = None, 0
     rc = lib().csa2_layer_group(ctypes.byref(a), _stream(stream))
     _check(rc, "csa2_layer_group")
+
+
+def csa2_prefill_index_scores(qI, w, kI, scores, d_status=None, stream=None):
+    """scores[q][j] = sum_h w[q][h] relu(qI[q][h] . kI[j]) on the tensor cores (qI [Q][8][128], kI [n][128])."""
+    _need(qI, "qI", torch.uint8, 3)
+    _need(w, "w", torch.float32, 2)
+    _need(kI, "kI", torch.uint8, 2)
+    _need(scores, "scores", torch.float32, 2)
+    Q, H_I, d_I = qI.shape
+    rc = lib().csa2_prefill_index_scores(_ptr(qI), _ptr(w), Q, H_I, d_I, _ptr(kI), kI.shape[0], _ptr(scores),
+                                         scores.shape[1], _ptr(d_status), _stream(stream))
+    _check(rc, "csa2_prefill_index_scores")
+
+
+def csa2_prefill_group(n_vis, codes, scales, kI, qI, w, idx, q_layers, swa_layers, swa_len, out_layers, ws,
+                       softmax_scale=None, d_status=None, events=None, stream=None):
+    """Encoder prefill group: indexer GEMM, per-query Top-K over n_vis[q] entries, attention per layer.
+    codes/scales/kI: one shared cache [n_keys][...]; swa_layers[l]: [Q + W - 1][512] chunk rows."""
+    _need(n_vis, "n_vis", torch.int64, 1)
+    _need(codes, "codes", torch.uint8, 2)
+    _need(scales, "scales", torch.uint8, 2)
+    _need(kI, "kI", torch.uint8, 2)
+    _need(qI, "qI", torch.uint8, 3)
+    _need(w, "w", torch.float32, 2)
+    _need(idx, "idx", torch.int32, 2)
+    _need(swa_len, "swa_len", torch.int32, 1)
+    _need(ws, "ws", torch.uint8)
+    L = len(q_layers)
+    for i in range(L):
+        _need(q_layers[i], f"q_layers[{i}]", torch.bfloat16, 3)
+        _need(swa_layers[i], f"swa_layers[{i}]", torch.bfloat16, 2)
+        _need(out_layers[i], f"out_layers[{i}]", torch.bfloat16, 3)
+    Q, H, d = q_layers[0].shape
+    a = PrefillArgs()
+    a.Q, a.n_reuse, a.H, a.d, a.H_I, a.d_I = Q, L - 1, H, d, qI.shape[1], qI.shape[2]
+    a.k, a.W = idx.shape[1], swa_layers[0].shape[0] - Q + 1
+    a.n_keys = codes.shape[0]
+    a.n_vis, a.codes, a.scales, a.kI = n_vis.data_ptr(), codes.data_ptr(), scales.data_ptr(), kI.data_ptr()
+    a.qI, a.w, a.idx = qI.data_ptr(), w.data_ptr(), idx.data_ptr()
+    qa = (_c_p * L)(*[t.data_ptr() for t in q_layers])
+    sa = (_c_p * L)(*[t.data_ptr() for t in swa_layers])
+    oa = (_c_p * L)(*[t.data_ptr() for t in out_layers])
+    a.q_layers, a.swa_layers, a.out_layers = qa, sa, oa
+    a.swa_len = swa_len.data_ptr()
+    a.softmax_scale = (1.0 / d ** 0.5) if softmax_scale is None else float(softmax_scale)
+    a.ws, a.ws_bytes = ws.data_ptr(), ws.numel()
+    a.d_status = d_status.data_ptr() if d_status is not None else None
+    if events:
+        ea = (_c_p * len(events))(*[e.cuda_event for e in events])
+        a.events, a.n_events = ea, len(events)
+    else:
+        a.events, a.n_events = None, 0
+    rc = lib().csa2_prefill_group(ctypes.byref(a), _stream(stream))
+    _check(rc, "csa2_prefill_group")
 
 
 def csa2_topk_noalloc(scores, n, n_max, k, idx_out, cand_pos=None, stream=None):

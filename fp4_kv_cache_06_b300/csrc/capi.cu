@@ -27,23 +27,30 @@ int launch_block_means(const uint8_t* kI, int B, int d_I, const int64_t* n, int6
                        int64_t n_cap, uint8_t* kbar, int32_t* st, cudaStream_t s);
 int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa, int W,
                       cudaStream_t s);
+int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
+                       int L, int W, int B, int d_I, const int64_t* pos, uint8_t* codes, uint8_t* scales,
+                       uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st, cudaStream_t s);
 int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
                       const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
                       int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
-                      uint32_t* hist, int32_t* st, cudaStream_t s);
+                      uint32_t* hist, TopkHdr* hdr, int topk_k, int32_t* st, cudaStream_t s);
 size_t topk_ws_bytes(int B);
 uint32_t* topk_ws_hist(void* ws);
+TopkHdr* topk_ws_hdr(void* ws, int B);
 int topk_prepare(void* ws, int B, cudaStream_t s);
 int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, const int64_t* n,
                 int len_div, int B, int64_t n_max, int k, int32_t* idx_out, void* ws, bool hist_ready,
                 cudaStream_t s);
 int topk_init_attributes();
+int prefill_init_attributes();
+int launch_prefill_index(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys, float* scores,
+                         int64_t stride, int32_t* st, cudaStream_t s);
 int attn_init_attributes();
 int attn_splits(int B, int H, int k, int W);
 size_t attn_ws_bytes(int B, int H, int k, int W);
 int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                       int64_t swa_seq_stride, int W, const int32_t* swa_len, float softmax_scale,
+                       int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
                        void* out, void* ws, int32_t* st, cudaStream_t s);
 
 // ---- bookkeeping --------------------------------------------------------------
@@ -62,6 +69,7 @@ static int ensure_init() {
   if (done_mask & (1ull << dev)) return CSA2_OK;
   int rc = topk_init_attributes();
   if (rc == CSA2_OK) rc = attn_init_attributes();
+  if (rc == CSA2_OK) rc = prefill_init_attributes();
   if (rc == CSA2_OK) done_mask |= (1ull << dev);
   return rc;
 }
@@ -104,7 +112,7 @@ static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, in
   if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
   if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
   if ((rc = launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, n_max, nullptr, 0,
-                              nullptr, topk_ws_hist(tk), st, s)) != CSA2_OK)
+                              nullptr, topk_ws_hist(tk), topk_ws_hdr(tk, B), k, st, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
   return launch_topk(scores, nullptr, n_max, n, 1, B, n_max, k, idx_out, tk, true, s);
@@ -119,7 +127,7 @@ static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, 
   void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)nb_max * 4);
   if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
   if ((rc = launch_index_scan(qI, w, kbar, kbar_seq_stride, n, kBlock, B, H_I, d_I, nb_max, scores, nb_max,
-                              nullptr, 0, nullptr, topk_ws_hist(tk), st, s)) != CSA2_OK)
+                              nullptr, 0, nullptr, topk_ws_hist(tk), topk_ws_hdr(tk, B), P, st, s)) != CSA2_OK)
     return rc;
   return launch_topk(scores, nullptr, nb_max, n, kBlock, B, nb_max, P, pool_out, tk, true, s);
 }
@@ -138,7 +146,7 @@ static int reindex_indexer(const uint8_t* qI, const float* w, const uint8_t* kI,
   // The pool scan writes every one of the P*8 slots of every row (absent
   // positions carry cand_pos -1), so Top-K takes all slots of each row.
   if (P > 0 && (rc = launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, INT64_MAX, scores, slots,
-                                       pool, P, cpos, topk_ws_hist(tk), st, s)) != CSA2_OK)
+                                       pool, P, cpos, topk_ws_hist(tk), topk_ws_hdr(tk, B), k, st, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
   return launch_topk(scores, cpos, slots, nullptr, 1, B, slots, k, idx_out, tk, true, s);
@@ -176,6 +184,11 @@ size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k, int3
     case CSA2_OP_INDEX_REINDEX: return ws_reindex(B, P);
     case CSA2_OP_FORM_POOL: return ws_form_pool(B, n_max);
     case CSA2_OP_SPARSE_ATTN: return attn_ws_bytes(B, H, k, 128);
+    case CSA2_OP_PREFILL_GROUP: {
+      // B = queries, n_max = entries: scores + Top-K + attention partials
+      size_t m = align256((size_t)B * (size_t)n_max * 4) + topk_ws_bytes(B);
+      return m + attn_ws_bytes(B, H, k, 128);
+    }
     case CSA2_OP_LAYER_GROUP: {
       size_t m = ws_index_full(B, n_max);
       const size_t r = ws_reindex(B, P), f = ws_form_pool(B, n_max), a = attn_ws_bytes(B, H, k, 128);
@@ -231,6 +244,24 @@ int csa2_append_swa(const void* x, int32_t B, int32_t d, const int64_t* pos, voi
   return launch_append_swa(x, B, d, pos, swa, W, static_cast<cudaStream_t>(stream));
 }
 
+int csa2_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
+                     int32_t L, int32_t W, int32_t B, int32_t d, int32_t d_I, const int64_t* pos,
+                     uint8_t* codes, uint8_t* scales, uint8_t* kI, uint8_t* kbar, int64_t n_cap,
+                     int32_t* d_status, void* stream) {
+  if (B < 0 || L < 0 || n_cap < 0 || (L > 0 && W <= 0)) return CSA2_ERR_INVALID_ARG;
+  if (d != 512 || (d_I != 64 && d_I != 128) || L > 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!kv_new || !kI_new || !pos || !codes || !scales || !kI || (L > 0 && (!swa_new || !swa)))
+    return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(kv_new) || !aligned16(codes) || !aligned16(scales) || ((uintptr_t)kI_new & 3) ||
+      ((uintptr_t)kI & 15) || (kbar && ((uintptr_t)kbar & 15)))
+    return CSA2_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l)
+    if (!swa_new[l] || !swa[l] || !aligned16(swa_new[l]) || !aligned16(swa[l])) return CSA2_ERR_INVALID_ARG;
+  return launch_append_step(kv_new, kI_new, swa_new, swa, L, W, B, d_I, pos, codes, scales, kI, kbar, n_cap,
+                            d_status, static_cast<cudaStream_t>(stream));
+}
+
 int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
                       const int64_t* n, int32_t B, int32_t H_I, int32_t d_I, int64_t n_max,
                       float* scores, int64_t scores_stride, int32_t* d_status, void* stream) {
@@ -239,7 +270,7 @@ int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int6
   if (B == 0 || n_max == 0) return CSA2_OK;
   if (!qI || !w || !kI || !n || !scores || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
   return launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, scores_stride,
-                           nullptr, 0, nullptr, nullptr, d_status, static_cast<cudaStream_t>(stream));
+                           nullptr, 0, nullptr, nullptr, nullptr, 0, d_status, static_cast<cudaStream_t>(stream));
 }
 
 int csa2_topk(const float* scores, const int32_t* cand_pos, int64_t scores_stride, const int64_t* n,
@@ -302,7 +333,7 @@ int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t* kI, int
 
 int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d, const uint8_t* codes,
                      const uint8_t* scales, int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx,
-                     int32_t k, const void* swa, int64_t swa_seq_stride, int32_t W,
+                     int32_t k, const void* swa, int64_t swa_seq_stride, int32_t W, int32_t swa_tail,
                      const int32_t* swa_len, float softmax_scale, void* out, void* ws, size_t ws_bytes,
                      int32_t* d_status, void* stream) {
   if (B < 0 || k < 0 || W < 0 || kv_seq_stride < 0 || swa_seq_stride < 0 || n_cap < 0) return CSA2_ERR_INVALID_ARG;
@@ -318,7 +349,7 @@ int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d, const uint8
   int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
   return launch_sparse_attn(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
-                            swa_len, softmax_scale, out, ws, d_status, static_cast<cudaStream_t>(stream));
+                            swa_tail != 0, swa_len, softmax_scale, out, ws, d_status, static_cast<cudaStream_t>(stream));
 }
 
 static cudaEvent_t group_event(const csa2_group_args* a, int i) {
@@ -370,10 +401,63 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   for (int l = 0; l <= a->n_reuse; ++l) {
     if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
     rc = launch_sparse_attn(a->q_layers[l], a->B, a->H, a->codes, a->scales, a->n_cap, a->n_cap, a->idx, a->k,
-                            a->swa_layers[l], a->W, a->W, a->swa_len, a->softmax_scale, a->out_layers[l], a->ws,
+                            a->swa_layers[l], a->W, a->W, 0, a->swa_len, a->softmax_scale, a->out_layers[l], a->ws,
                             a->d_status, s);
     if (rc != CSA2_OK) return rc;
     if ((rc = rec(group_event(a, 3 + l), s)) != CSA2_OK) return rc;
+  }
+  return CSA2_OK;
+}
+
+int csa2_prefill_index_scores(const uint8_t* qI, const float* w, int32_t Q, int32_t H_I, int32_t d_I,
+                              const uint8_t* kI, int64_t n_keys, float* scores, int64_t scores_stride,
+                              int32_t* d_status, void* stream) {
+  if (Q < 0 || n_keys < 0 || scores_stride < n_keys) return CSA2_ERR_INVALID_ARG;
+  if (H_I != 8 || d_I != 128 || n_keys > 0x7FFFFFFF || (int64_t)Q * 8 > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (Q == 0 || n_keys == 0) return CSA2_OK;
+  if (!qI || !w || !kI || !scores || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return launch_prefill_index(qI, w, Q, kI, n_keys, scores, scores_stride, d_status,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
+  if (!a) return CSA2_ERR_INVALID_ARG;
+  if (a->Q < 0 || a->n_reuse < 0 || a->n_keys < 0 || !a->q_layers || !a->swa_layers || !a->out_layers)
+    return CSA2_ERR_INVALID_ARG;
+  if (a->H_I != 8 || a->d_I != 128 || a->d != 512 || !topk_k_ok(a->k) || a->W < 0 || a->W > 128 ||
+      (a->H != 16 && a->H != 32 && a->H != 48 && a->H != 64) || a->n_keys > 0x7FFFFFFF)
+    return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (a->Q == 0) return CSA2_OK;
+  if (!a->n_vis || !a->codes || !a->scales || !a->kI || !a->qI || !a->w || !a->idx || !a->swa_len)
+    return CSA2_ERR_INVALID_ARG;
+  const size_t need = csa2_workspace_size(CSA2_OP_PREFILL_GROUP, a->Q, a->n_keys, a->k, 0, a->H);
+  if (!ws_ok(a->ws, a->ws_bytes, need)) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto ev = [&](int i) -> cudaEvent_t {
+    return (a->events && i < a->n_events) ? static_cast<cudaEvent_t>(a->events[i]) : nullptr;
+  };
+  float* scores = static_cast<float*>(a->ws);
+  void* tk = static_cast<char*>(a->ws) + align256((size_t)a->Q * (size_t)a->n_keys * 4);
+  void* aws = static_cast<char*>(tk) + topk_ws_bytes(a->Q);
+  // events: [0] before the indexer GEMM, [1] after it, [2] after Top-K, [3 + l] after layer l
+  if ((rc = rec(ev(0), s)) != CSA2_OK) return rc;
+  if ((rc = launch_prefill_index(a->qI, a->w, a->Q, a->kI, a->n_keys, scores, a->n_keys, a->d_status, s)) != CSA2_OK)
+    return rc;
+  if ((rc = rec(ev(1), s)) != CSA2_OK) return rc;
+  if ((rc = launch_topk(scores, nullptr, a->n_keys, a->n_vis, 1, a->Q, a->n_keys, a->k, a->idx, tk, false, s)) != CSA2_OK)
+    return rc;
+  if ((rc = rec(ev(2), s)) != CSA2_OK) return rc;
+  for (int l = 0; l <= a->n_reuse; ++l) {
+    if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
+    rc = launch_sparse_attn(a->q_layers[l], a->Q, a->H, a->codes, a->scales, 0, a->n_keys, a->idx, a->k,
+                            a->swa_layers[l], 1, a->W, 1, a->swa_len, a->softmax_scale, a->out_layers[l], aws,
+                            a->d_status, s);
+    if (rc != CSA2_OK) return rc;
+    if ((rc = rec(ev(3 + l), s)) != CSA2_OK) return rc;
   }
   return CSA2_OK;
 }

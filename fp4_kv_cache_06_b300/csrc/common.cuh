@@ -42,6 +42,82 @@ __device__ __forceinline__ int32_t cand_pos_of(uint64_t key) {
   return (int32_t)(~(uint32_t)(key & 0xFFFFFFFFull));
 }
 
+// ---- Top-K row header (workspace) -----------------------------------------
+struct TopkHdr {
+  uint32_t cnt;       // candidates appended by the compaction
+  uint32_t overflow;  // 1 = more than kCandCap would qualify: use the slow path
+  uint32_t done;      // CTAs of this row that have flushed their histogram
+  int32_t vbin;       // threshold bin of the level-0 histogram
+};
+constexpr int kTkThreads = 256;
+
+// Threshold bin of a 4096-bin histogram (counted from the top): the highest
+// bin v with (keys in bins >= v) >= k, or bin 0 when the row holds fewer than
+// k keys; *out_ge = keys in bins >= v. Needs all kTkThreads threads.
+__device__ __forceinline__ void find_threshold_bin(const uint32_t* __restrict__ h, int k, int* out_bin,
+                                                   uint32_t* out_ge) {
+  __shared__ uint32_t part[kTkThreads];
+  __shared__ int s_bin;
+  __shared__ uint32_t s_ge;
+  const int tid = threadIdx.x;
+  const int hi = kHistBins - 16 * tid;  // this thread's bins [hi-16, hi)
+  uint32_t loc = 0;
+#pragma unroll
+  for (int i = 1; i <= 16; ++i) loc += h[hi - i];
+  part[tid] = loc;
+  if (tid == 0) { s_bin = 0; s_ge = 0xFFFFFFFFu; }
+  __syncthreads();
+  for (int off = 1; off < kTkThreads; off <<= 1) {   // inclusive scan over threads
+    const uint32_t v = tid >= off ? part[tid - off] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  const uint32_t incl = part[tid], excl = incl - loc;
+  const uint32_t total = part[kTkThreads - 1];
+  if (total < (uint32_t)k) {
+    if (tid == 0) { s_bin = 0; s_ge = total; }
+  } else if (excl < (uint32_t)k && incl >= (uint32_t)k) {
+    uint32_t run = excl;
+    for (int i = 1; i <= 16; ++i) {
+      run += h[hi - i];
+      if (run >= (uint32_t)k) { s_bin = hi - i; s_ge = run; break; }
+    }
+  }
+  __syncthreads();
+  *out_bin = s_bin;
+  *out_ge = s_ge;
+}
+
+// End of a histogram-producing CTA (kTkThreads threads): add the CTA's
+// shared histogram into the row's global one; the last CTA of the row to
+// finish (counted with an atomic, no waiting) derives the threshold bin and
+// the overflow flag for the compaction step. `sh` is reused as scratch.
+__device__ __forceinline__ void topk_hist_flush(uint32_t* sh, uint32_t* __restrict__ ghist, TopkHdr* hdr,
+                                                int k, unsigned ctas_in_row) {
+  __shared__ int s_last;
+  __syncthreads();
+  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) {
+    const uint32_t v = sh[i];
+    if (v) atomicAdd(ghist + i, v);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&hdr->done, 1u) == ctas_in_row - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = __ldcg(ghist + i);
+  __syncthreads();
+  int vbin;
+  uint32_t ge;
+  find_threshold_bin(sh, k, &vbin, &ge);
+  if (threadIdx.x == 0) {
+    hdr->vbin = vbin;
+    hdr->overflow = ge > (uint32_t)kCandCap ? 1u : 0u;
+  }
+}
+
 // ---- FP8 / FP4 conversions (hardware RNE, satfinite) -----------------------
 // Two fp32 -> E4M3 bytes; `lo` lands in the low byte.
 __device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kScanThreads) k_index_scan(
     int64_t kI_seq_stride, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max,
     int64_t rows_per_cta, float* __restrict__ scores, int64_t scores_stride,
     const int32_t* __restrict__ pool, int P, int32_t* __restrict__ cand_pos,
-    uint32_t* __restrict__ hist, int32_t* st) {
+    uint32_t* __restrict__ hist, TopkHdr* __restrict__ hdr, int topk_k, int32_t* st) {
   constexpr int CH = DI / 64;                         // 16-byte chunks per row per thread
   __shared__ uint32_t sh_hist[kHistBins];
   const int b = blockIdx.y;
@@ -135,14 +135,7 @@ __global__ void __launch_bounds__(kScanThreads) k_index_scan(
       }
     }
   }
-  if (hist) {
-    __syncthreads();
-    uint32_t* gh = hist + (int64_t)b * kHistBins;
-    for (int i = tid; i < kHistBins; i += kScanThreads) {
-      const uint32_t v = sh_hist[i];
-      if (v) atomicAdd(gh + i, v);
-    }
-  }
+  if (hist) topk_hist_flush(sh_hist, hist + (int64_t)b * kHistBins, hdr + b, topk_k, gridDim.x);
 }
 
 // rows_per_cta: a multiple of the CTA's rows per iteration, sized so the
@@ -157,7 +150,7 @@ static int64_t scan_rows_per_cta(int B, int64_t rows) {
 int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
                       const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
                       int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
-                      uint32_t* hist, int32_t* st, cudaStream_t s) {
+                      uint32_t* hist, TopkHdr* hdr, int topk_k, int32_t* st, cudaStream_t s) {
   const bool use_pool = pool != nullptr;
   const int64_t rows = use_pool ? (int64_t)P * kBlock : n_max;
   if (rows == 0 || B == 0) return CSA2_OK;
@@ -166,7 +159,7 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
 #define CSA2_SCAN(DI_, POOL_)                                                                   \
   k_index_scan<DI_, POOL_><<<grid, kScanThreads, 0, s>>>(qI, w, kI, kI_seq_stride, n, len_div, H_I, n_max, \
                                                          per, scores, scores_stride, pool, P,     \
-                                                         cand_pos, hist, st)
+                                                         cand_pos, hist, hdr, topk_k, st)
   if (d_I == 128) {
     if (use_pool) CSA2_SCAN(128, true); else CSA2_SCAN(128, false);
   } else {

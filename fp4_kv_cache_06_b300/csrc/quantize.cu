@@ -16,8 +16,43 @@
 
 namespace csa2 {
 
-// One warp per bf16 row of 512 channels: lane l owns group l (channels
-// 16l..16l+15), i.e. one E4M3 scale and 8 bytes of codes.
+// One warp quantises one bf16 row of 512 channels: lane l owns group l
+// (channels 16l..16l+15), i.e. one E4M3 scale and 8 bytes of codes.
+__device__ __forceinline__ void quantize_row_warp(const uint4* __restrict__ xrow, uint8_t* __restrict__ crow,
+                                                  uint8_t* __restrict__ srow, int lane) {
+  const uint4 v0 = xrow[lane * 2];
+  const uint4 v1 = xrow[lane * 2 + 1];
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float f[16];
+  uint32_t sign_lo = 0, sign_hi = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    const uint32_t s0 = (w[j] >> 15) & 1u, s1 = (w[j] >> 31) & 1u;
+    if (j < 4) {
+      sign_lo |= (s0 << (8 * j + 3)) | (s1 << (8 * j + 7));
+    } else {
+      sign_hi |= (s0 << (8 * (j - 4) + 3)) | (s1 << (8 * (j - 4) + 7));
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+  const uint8_t sc = cvt_e4m3(__fdiv_rn(amax, 6.0f));
+  const float s = e4m3_to_f32(sc);
+  uint32_t lo = 0, hi = 0;
+  if (s > 0.f) {
+    float m[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m[j] = __fdiv_rn(fabsf(f[j]), s);
+    lo = cvt_e2m1x8(m) | sign_lo;
+    hi = cvt_e2m1x8(m + 8) | sign_hi;
+  }
+  *reinterpret_cast<uint2*>(crow + lane * 8) = make_uint2(lo, hi);
+  srow[lane] = sc;
+}
+
 __global__ void __launch_bounds__(256) k_quantize_fp4(const uint4* __restrict__ x, int B, int64_t rows,
                                                       const int64_t* __restrict__ pos,
                                                       uint8_t* __restrict__ codes,
@@ -34,39 +69,8 @@ __global__ void __launch_bounds__(256) k_quantize_fp4(const uint4* __restrict__ 
       if (lane == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
       continue;
     }
-    // 512 bf16 = 64 uint4 per row; lane reads its two
-    const uint4 v0 = x[r * 64 + lane * 2];
-    const uint4 v1 = x[r * 64 + lane * 2 + 1];
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float f[16];
-    uint32_t sign_lo = 0, sign_hi = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      f[2 * j] = __uint_as_float(w[j] << 16);
-      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-      const uint32_t s0 = (w[j] >> 15) & 1u, s1 = (w[j] >> 31) & 1u;
-      if (j < 4) {
-        sign_lo |= (s0 << (8 * j + 3)) | (s1 << (8 * j + 7));
-      } else {
-        sign_hi |= (s0 << (8 * (j - 4) + 3)) | (s1 << (8 * (j - 4) + 7));
-      }
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    const uint8_t sc = cvt_e4m3(__fdiv_rn(amax, 6.0f));
-    const float s = e4m3_to_f32(sc);
-    uint32_t lo = 0, hi = 0;
-    if (s > 0.f) {
-      float m[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) m[j] = __fdiv_rn(fabsf(f[j]), s);
-      lo = cvt_e2m1x8(m) | sign_lo;
-      hi = cvt_e2m1x8(m + 8) | sign_hi;
-    }
     const int64_t row = (int64_t)b * n_cap + p;
-    *reinterpret_cast<uint2*>(codes + row * 256 + lane * 8) = make_uint2(lo, hi);
-    scales[row * 32 + lane] = sc;
+    quantize_row_warp(x + r * 64, codes + row * 256, scales + row * 32, lane);
   }
 }
 
@@ -164,6 +168,69 @@ __global__ void k_append_swa(const uint4* __restrict__ x, int B, int d, const in
     swa[((int64_t)b * W + slot) * chunks + c] = x[(int64_t)b * chunks + c];
 }
 
+// ---- one decode token into every cache, one launch ---------------------------
+constexpr int kMaxStepLayers = 64;
+struct StepLayers {
+  const uint4* src[kMaxStepLayers];   // [B][d] bf16 new SWA rows
+  uint4* dst[kMaxStepLayers];         // [B][W][d] bf16 rings
+};
+
+// One warp per task; task = b * (2 + L) + kind: kind 0 quantises the main-KV
+// row, kind 1 appends the indexer key and refreshes its block mean (the new
+// key is taken from the input, the block's earlier keys from the cache),
+// kind 2 + l writes layer l's SWA row into slot pos % W.
+__global__ void __launch_bounds__(256) k_append_step(const uint4* __restrict__ kv_new,
+                                                     const uint8_t* __restrict__ kI_new, StepLayers layers,
+                                                     int L, int W, int B, int d_I,
+                                                     const int64_t* __restrict__ pos, uint8_t* __restrict__ codes,
+                                                     uint8_t* __restrict__ scales, uint8_t* __restrict__ kI,
+                                                     uint8_t* __restrict__ kbar, int64_t n_cap, int32_t* st) {
+  const int lane = threadIdx.x & 31;
+  const int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int per = 2 + L;
+  if (task >= (int64_t)B * per) return;
+  const int b = (int)(task / per), kind = (int)(task - (int64_t)b * per);
+  const int64_t p = pos[b];
+  if (p < 0 || p >= n_cap) {
+    if (lane == 0 && kind == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (kind == 0) {
+    const int64_t row = (int64_t)b * n_cap + p;
+    quantize_row_warp(kv_new + (int64_t)b * 64, codes + row * 256, scales + row * 32, lane);
+  } else if (kind == 1) {
+    const uint8_t* kseq = kI + (int64_t)b * n_cap * d_I;
+    const int c = lane * 4;
+    if (c < d_I) {
+      const uint32_t nv = *reinterpret_cast<const uint32_t*>(kI_new + (int64_t)b * d_I + c);
+      *reinterpret_cast<uint32_t*>(kI + ((int64_t)b * n_cap + p) * d_I + c) = nv;
+      if (kbar != nullptr) {
+        const int64_t j = p / kBlock;
+        float acc[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[u] = e4m3_to_f32((uint8_t)(nv >> (8 * u)));
+        for (int64_t t = j * kBlock; t < p; ++t) {
+          const uint32_t v = *reinterpret_cast<const uint32_t*>(kseq + t * d_I + c);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc[u] += e4m3_to_f32((uint8_t)(v >> (8 * u)));
+        }
+        const float cnt = (float)(p - j * kBlock + 1);
+        const uint16_t lo = cvt_e4m3x2(__fdiv_rn(acc[0], cnt), __fdiv_rn(acc[1], cnt));
+        const uint16_t hi = cvt_e4m3x2(__fdiv_rn(acc[2], cnt), __fdiv_rn(acc[3], cnt));
+        const int64_t nbc = (n_cap + kBlock - 1) / kBlock;
+        *reinterpret_cast<uint32_t*>(kbar + ((int64_t)b * nbc + j) * d_I + c) = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+    }
+  } else {
+    const int l = kind - 2;
+    const int64_t slot = p % W;
+    const uint4* src = layers.src[l] + (int64_t)b * 64;
+    uint4* dst = layers.dst[l] + ((int64_t)b * W + slot) * 64;
+    dst[lane] = src[lane];
+    dst[lane + 32] = src[lane + 32];
+  }
+}
+
 // ---- host launchers -----------------------------------------------------
 int launch_quantize_fp4(const void* x, int B, int64_t rows, const int64_t* pos, uint8_t* codes,
                         uint8_t* scales, int64_t n_cap, int32_t* st, cudaStream_t s) {
@@ -215,4 +282,22 @@ int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa
   return launch_status();
 }
 
+}  // namespace csa2
+
+namespace csa2 {
+int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
+                       int L, int W, int B, int d_I, const int64_t* pos, uint8_t* codes, uint8_t* scales,
+                       uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st, cudaStream_t s) {
+  if (L > kMaxStepLayers) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  StepLayers ly;
+  for (int l = 0; l < kMaxStepLayers; ++l) {
+    ly.src[l] = l < L ? reinterpret_cast<const uint4*>(swa_new[l]) : nullptr;
+    ly.dst[l] = l < L ? reinterpret_cast<uint4*>(swa[l]) : nullptr;
+  }
+  const int64_t warps = (int64_t)B * (2 + L);
+  k_append_step<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(reinterpret_cast<const uint4*>(kv_new), kI_new, ly, L,
+                                                            W, B, d_I, pos, codes, scales, kI, kbar, n_cap, st);
+  count_launch();
+  return launch_status();
+}
 }  // namespace csa2

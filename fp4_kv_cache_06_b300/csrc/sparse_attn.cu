@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(128 * MT, 1) k_sparse_attn(
     const __nv_bfloat16* __restrict__ q, const uint8_t* __restrict__ codes,
     const uint8_t* __restrict__ scales, int64_t kv_seq_stride, int64_t n_cap,
     const int32_t* __restrict__ idx, int k, const __nv_bfloat16* __restrict__ swa,
-    int64_t swa_seq_stride, int W, const int32_t* __restrict__ swa_len, float scale_log2,
+    int64_t swa_seq_stride, int W, int swa_tail, const int32_t* __restrict__ swa_len, float scale_log2,
     int splits, int tiles_per_split, __nv_bfloat16* __restrict__ out, float* __restrict__ part_o,
     float* __restrict__ part_ml, int32_t* st) {
   using L = AttnSmem<MT>;
@@ -113,7 +113,8 @@ __global__ void __launch_bounds__(128 * MT, 1) k_sparse_attn(
         if (p >= 0 && p < n_cap) src = (int64_t)b * kv_seq_stride + p;
         else if (p >= n_cap) report(st, CSA2_ERR_DEVICE_BOUNDS);
       } else if (j - k < slen) {
-        src = (int64_t)b * swa_seq_stride + (j - k);
+        // valid SWA rows: the first slen of the W-row window, or its last slen
+        src = (int64_t)b * swa_seq_stride + (swa_tail ? W - slen : 0) + (j - k);
         kind = 1;
       }
       sSrc[tid] = src;
@@ -338,7 +339,7 @@ size_t attn_ws_bytes(int B, int H, int k, int W) {
 template <int MT>
 static int launch_attn_mt(const void* q, int B, const uint8_t* codes, const uint8_t* scales,
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k,
-                          const void* swa, int64_t swa_seq_stride, int W, const int32_t* swa_len,
+                          const void* swa, int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len,
                           float softmax_scale, void* out, void* ws, int32_t* st, cudaStream_t s) {
   constexpr int H = 16 * MT;
   const int smem = AttnSmem<MT>::kBytes;
@@ -356,7 +357,7 @@ static int launch_attn_mt(const void* q, int B, const uint8_t* codes, const uint
   dim3 grid((unsigned)splits, (unsigned)B);
   k_sparse_attn<MT><<<grid, 128 * MT, smem, s>>>(
       reinterpret_cast<const __nv_bfloat16*>(q), codes, scales, kv_seq_stride, n_cap, idx, k,
-      reinterpret_cast<const __nv_bfloat16*>(swa), swa_seq_stride, W, swa_len, scale_log2, splits, tps,
+      reinterpret_cast<const __nv_bfloat16*>(swa), swa_seq_stride, W, swa_tail, swa_len, scale_log2, splits, tps,
       reinterpret_cast<__nv_bfloat16*>(out), part_o, part_ml, st);
   count_launch();
   int rc = launch_status();
@@ -378,14 +379,14 @@ int attn_init_attributes() {
 
 int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                       int64_t swa_seq_stride, int W, const int32_t* swa_len, float softmax_scale,
+                       int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
                        void* out, void* ws, int32_t* st, cudaStream_t s) {
   if (B == 0) return CSA2_OK;
   switch (H) {
-    case 16: return launch_attn_mt<1>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_len, softmax_scale, out, ws, st, s);
-    case 32: return launch_attn_mt<2>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_len, softmax_scale, out, ws, st, s);
-    case 48: return launch_attn_mt<3>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_len, softmax_scale, out, ws, st, s);
-    case 64: return launch_attn_mt<4>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_len, softmax_scale, out, ws, st, s);
+    case 16: return launch_attn_mt<1>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_tail, swa_len, softmax_scale, out, ws, st, s);
+    case 32: return launch_attn_mt<2>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_tail, swa_len, softmax_scale, out, ws, st, s);
+    case 48: return launch_attn_mt<3>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_tail, swa_len, softmax_scale, out, ws, st, s);
+    case 64: return launch_attn_mt<4>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_tail, swa_len, softmax_scale, out, ws, st, s);
     default: return CSA2_ERR_UNSUPPORTED_SHAPE;
   }
 }

@@ -25,11 +25,6 @@
 
 namespace csa2 {
 
-struct TopkHdr {
-  uint32_t cnt;       // candidates appended by the compaction
-  uint32_t overflow;  // 1 = more than kCandCap would qualify: use the slow path
-  uint32_t pad[2];
-};
 
 // Workspace layout (all offsets 256-byte aligned):
 //   hist [B][kHistBins] u32 | hdr [B] TopkHdr | cand [B][kCandCap] u64
@@ -54,8 +49,8 @@ static TopkWs topk_ws(void* ws, int B) {
   return r;
 }
 uint32_t* topk_ws_hist(void* ws) { return static_cast<uint32_t*>(ws); }
+TopkHdr* topk_ws_hdr(void* ws, int B) { return topk_ws(ws, B).hdr; }
 
-constexpr int kTkThreads = 256;
 
 // Candidates of row b: the first ceil(n[b] / len_div) entries, at most n_max
 // (n == NULL: every row has n_max entries).
@@ -71,7 +66,8 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_hist(const float* __restric
                                                           const int32_t* __restrict__ cand_pos,
                                                           int64_t stride, const int64_t* __restrict__ n,
                                                           int len_div, int64_t n_max, int64_t per,
-                                                          uint32_t* __restrict__ hist) {
+                                                          uint32_t* __restrict__ hist, TopkHdr* __restrict__ hdr,
+                                                          int k) {
   __shared__ uint32_t sh[kHistBins];
   const int b = blockIdx.y;
   for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = 0;
@@ -84,69 +80,19 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_hist(const float* __restric
     if (cp && cp[i] < 0) continue;
     atomicAdd(&sh[score_key(s[i]) >> 20], 1u);
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads)
-    if (sh[i]) atomicAdd(hist + (int64_t)b * kHistBins + i, sh[i]);
-}
-
-// Threshold bin: the highest bin v with (count of keys in bins >= v) >= k,
-// or bin 0 when the row has fewer than k keys. Also returns that count.
-// 256 threads, each owning 16 consecutive bins counted from the top.
-__device__ void find_threshold_bin(const uint32_t* __restrict__ h, int k, int* out_bin,
-                                   uint32_t* out_ge) {
-  __shared__ uint32_t part[kTkThreads];
-  __shared__ int s_bin;
-  __shared__ uint32_t s_ge;
-  const int tid = threadIdx.x;
-  const int hi = kHistBins - 16 * tid;  // bins [hi-16, hi)
-  uint32_t loc = 0;
-#pragma unroll
-  for (int i = 1; i <= 16; ++i) loc += h[hi - i];
-  part[tid] = loc;
-  if (tid == 0) { s_bin = 0; s_ge = 0xFFFFFFFFu; }
-  __syncthreads();
-  // inclusive scan over threads (Hillis-Steele in shared memory)
-  for (int off = 1; off < kTkThreads; off <<= 1) {
-    const uint32_t v = tid >= off ? part[tid - off] : 0;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
-  }
-  const uint32_t incl = part[tid], excl = incl - loc;
-  const uint32_t total = part[kTkThreads - 1];
-  if (total < (uint32_t)k) {
-    if (tid == 0) { s_bin = 0; s_ge = total; }
-  } else if (excl < (uint32_t)k && incl >= (uint32_t)k) {
-    uint32_t run = excl;
-    for (int i = 1; i <= 16; ++i) {
-      run += h[hi - i];
-      if (run >= (uint32_t)k) { s_bin = hi - i; s_ge = run; break; }
-    }
-  }
-  __syncthreads();
-  *out_bin = s_bin;
-  *out_ge = s_ge;
+  topk_hist_flush(sh, hist + (int64_t)b * kHistBins, hdr + b, k, gridDim.x);
 }
 
 // ---- step 2 ----------------------------------------------------------------
 __global__ void __launch_bounds__(kTkThreads) k_topk_compact(const float* __restrict__ scores,
                                                              const int32_t* __restrict__ cand_pos,
                                                              int64_t stride, const int64_t* __restrict__ n,
-                                                             int len_div, int64_t n_max, int64_t per, int k,
-                                                             const uint32_t* __restrict__ hist,
+                                                             int len_div, int64_t n_max, int64_t per,
                                                              TopkHdr* __restrict__ hdr,
                                                              uint64_t* __restrict__ cand) {
-  __shared__ uint32_t sh[kHistBins];
   const int b = blockIdx.y;
-  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = hist[(int64_t)b * kHistBins + i];
-  __syncthreads();
-  int vbin;
-  uint32_t ge;
-  find_threshold_bin(sh, k, &vbin, &ge);
-  if (ge > (uint32_t)kCandCap) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) hdr[b].overflow = 1u;
-    return;
-  }
+  if (hdr[b].overflow) return;
+  const int vbin = hdr[b].vbin;
   const int64_t nb = row_len(n, b, len_div, n_max);
   const int64_t c0 = (int64_t)blockIdx.x * per, c1 = min(c0 + per, nb);
   const float* s = scores + (int64_t)b * stride;
@@ -173,7 +119,7 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_compact(const float* __rest
       basei = __shfl_sync(0xffffffffu, basei, leader);
       if (take) {
         const uint32_t slot = basei + __popc(m & ((1u << lane) - 1u));
-        if (slot < (uint32_t)kCandCap) out[slot] = key;  // always true: ge <= kCandCap
+        if (slot < (uint32_t)kCandCap) out[slot] = key;  // always true: the row did not overflow
       }
     }
   }
@@ -215,9 +161,14 @@ __device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
     for (int i = tid; i < 256; i += kFinThreads) h256[i] = 0;
     __syncthreads();
     const int64_t m = src.size();
-    for (int64_t i = tid; i < m; i += kFinThreads) {
-      uint64_t key;
-      if (src.get(i, key) && (key & mask) == prefix) atomicAdd(&h256[(key >> shift) & 255], 1u);
+    const int lane = tid & 31;
+    for (int64_t i0 = 0; i0 < m; i0 += kFinThreads) {
+      const int64_t i = i0 + tid;
+      uint64_t key = 0;
+      const bool ok = i < m && src.get(i, key) && (key & mask) == prefix;
+      const uint32_t dgt = ok ? (uint32_t)((key >> shift) & 255) : 256u;
+      const uint32_t peers = __match_any_sync(0xffffffffu, dgt);   // lanes holding the same digit
+      if (ok && lane == __ffs(peers) - 1) atomicAdd(&h256[dgt], (uint32_t)__popc(peers));
     }
     __syncthreads();
     if (tid < 32) {
@@ -283,10 +234,19 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
   for (int i = tid; i < np; i += kFinThreads) sel[i] = 0x7FFFFFFF;
   __syncthreads();
   const int64_t m = src.size();
-  for (int64_t i = tid; i < m; i += kFinThreads) {
-    uint64_t key;
-    if (src.get(i, key) && key >= thr) {
-      const uint32_t slot = atomicAdd(&s_cnt, 1u);
+  const int lane = tid & 31;
+  for (int64_t i0 = 0; i0 < m; i0 += kFinThreads) {
+    const int64_t i = i0 + tid;
+    uint64_t key = 0;
+    const bool take = i < m && src.get(i, key) && key >= thr;
+    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+    uint32_t base = 0;
+    if (bal) {
+      if (lane == __ffs(bal) - 1) base = atomicAdd(&s_cnt, (uint32_t)__popc(bal));
+      base = __shfl_sync(0xffffffffu, base, __ffs(bal) - 1);
+    }
+    if (take) {
+      const uint32_t slot = base + __popc(bal & ((1u << lane) - 1u));
       if (slot < (uint32_t)k) sel[slot] = cand_pos_of(key);
     }
   }
@@ -359,11 +319,11 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
   dim3 grid((unsigned)((n_max + per - 1) / per > 0 ? (n_max + per - 1) / per : 1), (unsigned)B);
   if (!hist_ready) {
     if ((rc = topk_prepare(ws, B, s)) != CSA2_OK) return rc;
-    k_topk_hist<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, w.hist);
+    k_topk_hist<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, w.hist, w.hdr, k);
     count_launch();
     if ((rc = launch_status()) != CSA2_OK) return rc;
   }
-  k_topk_compact<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, k, w.hist, w.hdr,
+  k_topk_compact<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, w.hdr,
                                              w.cand);
   count_launch();
   if ((rc = launch_status()) != CSA2_OK) return rc;

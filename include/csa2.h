@@ -85,7 +85,8 @@ enum csa2_op {
   CSA2_OP_INDEX_REINDEX = 3, /* csa2_index_reindex                         */
   CSA2_OP_FORM_POOL = 4,     /* csa2_form_pool                             */
   CSA2_OP_SPARSE_ATTN = 5,   /* csa2_sparse_attn (split-K partials)        */
-  CSA2_OP_LAYER_GROUP = 6    /* csa2_layer_group (max of the above)        */
+  CSA2_OP_LAYER_GROUP = 6,   /* csa2_layer_group (max of the above)        */
+  CSA2_OP_PREFILL_GROUP = 7  /* csa2_prefill_group: B = queries, n_max = entries */
 };
 
 /* Bytes of workspace an op needs for B rows of at most n_max candidates,
@@ -135,6 +136,20 @@ CSA2_API int csa2_block_means(const uint8_t* kI, int32_t B, int32_t d_I,
  *   x [B][d] bf16; pos [B] int64 device; swa [B][W][d] bf16 */
 CSA2_API int csa2_append_swa(const void* x, int32_t B, int32_t d, const int64_t* pos,
                     void* swa, int32_t W, void* stream);
+
+/* Append one decode token to every cache of a layer stack in ONE launch:
+ * the main-KV row x_b (FP4, exactly as csa2_quantize_kv_fp4), the indexer
+ * key (with its block mean, exactly as csa2_append_indexer_k; kbar may be
+ * NULL) and each layer's SWA row (as csa2_append_swa), all at pos[b].
+ *   kv_new [B][d] bf16; kI_new [B][d_I] u8
+ *   swa_new, swa: HOST arrays of L device pointers ([B][d] bf16 new rows,
+ *   [B][W][d] bf16 rings); L <= 64. Other arrays as in the calls above. */
+CSA2_API int csa2_append_step(const void* kv_new, const uint8_t* kI_new,
+                              const void* const* swa_new, void* const* swa,
+                              int32_t L, int32_t W, int32_t B, int32_t d,
+                              int32_t d_I, const int64_t* pos, uint8_t* codes,
+                              uint8_t* scales, uint8_t* kI, uint8_t* kbar,
+                              int64_t n_cap, int32_t* d_status, void* stream);
 
 /* ---- a3: indexer scores [CSA2] ------------------------------------------ */
 /* Raw indexer scan: scores[b][t] = sum_h w[b][h] * relu(qI[b][h] . kI[b][t])
@@ -234,16 +249,21 @@ CSA2_API int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t
  *   codes/scales row (b,t) at (b*kv_seq_stride + t); t must be < n_cap
  *            (checked: CSA2_ERR_DEVICE_BOUNDS, key skipped)
  *   idx      [B][k] int32
- *   swa      rows of sequence b start at swa + b*swa_seq_stride*d (W = 128
- *            for decode rings; prefill passes stride 1 so query b's window
- *            is rows b .. b+swa_len[b]-1 of the chunk's SWA array)
- *   swa_len  [B] int32 device, each <= W
+ *   swa      the W-row SWA window of sequence b starts at row b*swa_seq_stride
+ *            (decode rings: stride W; a prefill chunk: stride 1, the array
+ *            holding the rows of tokens p0-W+1 .. p0+B-1 for queries at
+ *            tokens p0 .. p0+B-1)
+ *   swa_len  [B] int32 device, each <= W: keys present in the window
+ *   swa_tail 0: the present keys are the window's first swa_len rows (a
+ *            ring that has not wrapped yet); 1: its last swa_len rows (a
+ *            prefill window cut off at the start of the sequence)
  * Workspace: CSA2_OP_SPARSE_ATTN. */
 CSA2_API int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d,
                      const uint8_t* codes, const uint8_t* scales,
                      int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx,
                      int32_t k, const void* swa, int64_t swa_seq_stride,
-                     int32_t W, const int32_t* swa_len, float softmax_scale,
+                     int32_t W, int32_t swa_tail, const int32_t* swa_len,
+                     float softmax_scale,
                      void* out, void* ws, size_t ws_bytes, int32_t* d_status,
                      void* stream);
 
@@ -289,6 +309,59 @@ typedef struct csa2_group_args {
  * attention for the first layer and each Reuse layer with the group's
  * Top-K, each with its own main Q and SWA KV. */
 CSA2_API int csa2_layer_group(const csa2_group_args* args, void* stream);
+
+/* ---- prefill chunk (encoder Full + Reuse layers) [CSA2][CED] ------------ */
+/* Prefill indexer scores on the tensor cores: for every query q of a chunk
+ * and every compressed entry j < n_keys (one cache shared by all queries),
+ * scores[q][j] = sum_h w[q][h] * relu(qI[q][h] . kI[j]), FP8 E4M3 products
+ * accumulated in fp32 (tcgen05 FP8 GEMM, TMA-fed). Entries past a query's
+ * causal limit are scored too; the causal rule is applied by giving the
+ * Top-K each query's visible count.
+ *   qI [Q][8][128] u8; w [Q][8] fp32; kI [n_keys][128] u8
+ *   scores [Q][scores_stride] fp32, scores_stride >= n_keys
+ * Supported: H_I = 8, d_I = 128. */
+CSA2_API int csa2_prefill_index_scores(const uint8_t* qI, const float* w,
+                                       int32_t Q, int32_t H_I, int32_t d_I,
+                                       const uint8_t* kI, int64_t n_keys,
+                                       float* scores, int64_t scores_stride,
+                                       int32_t* d_status, void* stream);
+
+/* Arguments of csa2_prefill_group. Pointers are device pointers unless noted. */
+typedef struct csa2_prefill_args {
+  int32_t Q;             /* queries (tokens) in the chunk                      */
+  int32_t n_reuse;       /* Reuse layers after the Full layer                  */
+  int32_t H, d, H_I, d_I, k, W;
+  int64_t n_keys;        /* compressed main-KV entries in the shared cache     */
+  const int64_t* n_vis;  /* [Q] entries visible to each query: an entry of
+                            `ratio` tokens is visible once its last token is
+                            at or before the query, i.e. floor((p+1)/ratio)   */
+  const uint8_t* codes;  /* [n_keys][d/2]                                      */
+  const uint8_t* scales; /* [n_keys][d/16]                                     */
+  const uint8_t* kI;     /* [n_keys][d_I]                                      */
+  const uint8_t* qI;     /* [Q][H_I][d_I]                                      */
+  const float* w;        /* [Q][H_I]                                           */
+  int32_t* idx;          /* [Q][k] Top-K of each query (written)               */
+  const void* const* q_layers;    /* HOST array [1+n_reuse] of [Q][H][d] bf16 */
+  const void* const* swa_layers;  /* HOST array [1+n_reuse] of the chunk's SWA
+                                     rows [Q + W - 1][d] bf16: query q's window
+                                     is rows q .. q + swa_len[q] - 1          */
+  const int32_t* swa_len;         /* [Q] (<= W)                               */
+  void* const* out_layers;        /* HOST array [1+n_reuse] of [Q][H][d] bf16 */
+  float softmax_scale;
+  void* ws;              /* workspace, CSA2_OP_PREFILL_GROUP                   */
+  size_t ws_bytes;
+  int32_t* d_status;     /* optional                                           */
+  void* const* events;   /* optional HOST array of cudaEvent_t: [0] before the
+                            indexer GEMM, [1] after it, [2] after Top-K,
+                            [3 + l] after layer l's attention                 */
+  int32_t n_events;
+} csa2_prefill_args;
+
+/* One encoder group over a prefill chunk: the Full layer's indexer GEMM
+ * (csa2_prefill_index_scores), Top-k of each query over its visible entries,
+ * then sparse attention of the Full layer and of each Reuse layer with those
+ * indices, every layer with its own Q and SWA rows. */
+CSA2_API int csa2_prefill_group(const csa2_prefill_args* args, void* stream);
 
 #ifdef __cplusplus
 }

@@ -59,6 +59,8 @@ def test_host_validation_rejects_bad_arguments():
     assert lib.csa2_index_scores(nul, nul, nul, 0, nul, 1, 8, 96, 10, nul, 10, nul, nul) == 2    # d_I
     assert lib.csa2_topk(nul, nul, 10, nul, 1, 10, 4096, nul, nul, 0, nul) == 2                 # k too large
     assert lib.csa2_topk(ctypes.c_void_p(256), nul, 10, ctypes.c_void_p(256), 1, 10, 8, ctypes.c_void_p(256), nul, 0, nul) == 3  # no workspace
-    assert lib.csa2_sparse_attn(nul, 1, 24, 512, nul, nul, 0, 0, nul, 512, nul, 128, 128, nul, 0.1, nul, nul, 0, nul, nul) == 2  # H
-    assert lib.csa2_sparse_attn(nul, 1, 64, 512, nul, nul, 0, 0, nul, 512, nul, 128, 129, nul, 0.1, nul, nul, 0, nul, nul) == 2  # W
+    assert lib.csa2_sparse_attn(nul, 1, 24, 512, nul, nul, 0, 0, nul, 512, nul, 128, 128, 0, nul, 0.1, nul, nul, 0, nul, nul) == 2  # H
+    assert lib.csa2_sparse_attn(nul, 1, 64, 512, nul, nul, 0, 0, nul, 512, nul, 128, 129, 0, nul, 0.1, nul, nul, 0, nul, nul) == 2  # W
+    assert lib.csa2_prefill_index_scores(nul, nul, 4, 4, 128, nul, 100, nul, 100, nul, nul) == 2  # H_I must be 8
+    assert lib.csa2_prefill_group(None, nul) == 1
     assert lib.csa2_layer_group(None, nul) == 1

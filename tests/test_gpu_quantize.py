@@ -126,3 +126,41 @@ def test_swa_append_ring_slot():
     for b, p in enumerate([0, 127, 1000003]):
         assert torch.equal(swa[b, p % W], x[b])
         assert int((swa[b].abs().sum(-1) > 0).sum()) == 1
+
+
+@pytest.mark.parametrize("d_I,L", [(128, 4), (64, 1), (128, 20)])
+def test_append_step_matches_individual_appends(d_I, L):
+    """The fused one-launch append equals the three separate appends, bit for bit."""
+    B, n_cap, W = 5, 64, 128
+    pos_list = [0, 7, 8, 13, 63]
+    pos = torch.tensor(pos_list, dtype=torch.int64, device=DEV)
+    base_kI = synth.indexer_keys_e4m3((B, n_cap, d_I), seed=8).to(DEV)
+    kv_new = synth.normal_bf16((B, 512), seed=8, stream="kv_new").to(DEV)
+    kI_new = synth.indexer_keys_e4m3((B, 1, d_I), seed=9).to(DEV)[:, 0].contiguous()
+    swa_new = [synth.normal_bf16((B, 512), seed=8, stream="swa_new", sub=l).to(DEV) for l in range(L)]
+
+    def caches():
+        kI = base_kI.clone()
+        kbar = torch.zeros((B, n_cap // 8, d_I), dtype=torch.uint8, device=DEV)
+        codes = torch.zeros((B, n_cap, 256), dtype=torch.uint8, device=DEV)
+        scales = torch.zeros((B, n_cap, 32), dtype=torch.uint8, device=DEV)
+        swa = [torch.zeros((B, W, 512), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+        return kI, kbar, codes, scales, swa
+
+    a = caches()
+    csa2.csa2_append_step(kv_new, kI_new, swa_new, a[4], pos, a[2], a[3], a[0], a[1])
+    b = caches()
+    csa2.csa2_quantize_kv_fp4(kv_new[:, None].contiguous(), b[2], b[3], pos=pos)
+    csa2.csa2_append_indexer_k(kI_new[:, None].contiguous(), b[0], b[1], pos=pos)
+    for l in range(L):
+        csa2.csa2_append_swa(swa_new[l], pos, b[4][l])
+    torch.cuda.synchronize()
+    for x, y in zip(a[:4], b[:4]):
+        assert torch.equal(x, y)
+    for x, y in zip(a[4], b[4]):
+        assert torch.equal(x, y)
+    # and the block means equal the oracle's over the appended cache
+    kI_np = u8(a[0])
+    for i, p in enumerate(pos_list):
+        ref = oracle.block_means(kI_np[i], p + 1)
+        np.testing.assert_array_equal(u8(a[1])[i, p // 8], ref[p // 8])
