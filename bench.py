@@ -84,48 +84,41 @@ def max_over_ranks(x, world, device):
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
-_POLLER = r"""
-import sys, time
-import pynvml
-pynvml.nvmlInit()
-uuid = sys.argv[1]
-try:
-    h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
-except Exception:
-    h = pynvml.nvmlDeviceGetHandleByIndex(int(sys.argv[2]))
-print("max", pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM), flush=True)
-while True:
-    sm = pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM)
-    r = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
-    print(sm, r, flush=True)
-    time.sleep(0.002)
-"""
-
-
 class ClockSampler:
-    """Samples the SM clock and the clock-event (throttle) reasons of one GPU
-    every ~2 ms from a separate process while the timed region runs
-    (read-only NVML queries; no GPU setting is changed)."""
-    HW_SLOWDOWN, SW_POWER_CAP, SW_THERMAL, HW_THERMAL = 0x8, 0x4, 0x20, 0x40
+    """Samples SM clock and clock-event (throttle) reasons of one GPU every
+    20 ms with nvidia-smi (read-only queries; no GPU setting is changed).
+    Start it before the warm-up; mark() the timed window; summary() reports
+    the samples inside the window, or, if the window was too short to hold
+    one, those of the whole warm-up + timed span (flagged as such)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.out = ""
+        self.window = None
 
-    def __enter__(self):
+    def start(self):
         try:
             import torch
-            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.gpu).uuid)
-            self.proc = subprocess.Popen([sys.executable, "-c", _POLLER, uuid, str(self.gpu)],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            time.sleep(0.5)                      # let the poller start before the timed region
+            idx = str(self.gpu)
+            env = dict(os.environ)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, env=env)
+            time.sleep(1.0)
         except Exception:
             self.proc = None
         return self
 
-    def __exit__(self, *a):
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
         if self.proc is not None:
+            time.sleep(0.05)
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)
@@ -133,24 +126,33 @@ class ClockSampler:
                 self.proc.kill()
                 self.out = ""
 
+    @staticmethod
+    def _epoch(ts):
+        import datetime
+        try:
+            return datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        sm_max, samples = None, []
+        rows, sm_max = [], None
         for ln in self.out.splitlines():
-            parts = ln.split()
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 7:
+                continue
             try:
-                if parts[0] == "max":
-                    sm_max = float(parts[1])
-                else:
-                    samples.append((float(parts[0]), int(parts[1])))
-            except (ValueError, IndexError):
-                pass
-        if not samples:
+                rows.append((self._epoch(p[0]), float(p[1]), [v.lower().startswith("active") for v in p[3:7]]))
+                sm_max = float(p[2])
+            except ValueError:
+                continue
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": sm_max, "reasons": ["unavailable"], "samples": 0}
-        names = {self.HW_SLOWDOWN: "hw_slowdown", self.HW_THERMAL: "hw_thermal_slowdown",
-                 self.SW_THERMAL: "sw_thermal_slowdown", self.SW_POWER_CAP: "sw_power_cap"}
-        seen = {nm for _, r in samples for bit, nm in names.items() if r & bit}
-        return {"sm_mhz": statistics.median(x for x, _ in samples), "sm_max_mhz": sm_max,
-                "reasons": sorted(seen), "samples": len(samples)}
+        inside = [r for r in rows if self.window and r[0] is not None and self.window[0] <= r[0] <= self.window[1]]
+        use, span = (inside, "timed") if inside else (rows, "warmup+timed")
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = sorted({n for _, _, fl in use for n, f in zip(names, fl) if f})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": sm_max, "reasons": seen,
+                "samples": len(use), "span": span}
 
 
 # ---------------------------------------------------------------------------
@@ -332,12 +334,13 @@ def run_prefill(args, world, rank, local):
     torch.cuda.set_device(dev)
     cfg = synth.get_config(args.config)
     wl = PrefillWorkload(cfg, dev, seed=1234 + 7919 * rank, queries=args.batch)
+    clk = ClockSampler(local).start()
     for _ in range(args.warmup):
         wl.step()
     torch.cuda.synchronize()
 
     def mk():
-        e = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True, external=True)
         e.record()
         return e
     nev = 3 + wl.layers
@@ -345,17 +348,23 @@ def run_prefill(args, world, rank, local):
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
     torch.cuda.synchronize()
     launches0 = csa2.launch_count()
-    barrier(world)
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
         for i in range(args.steps):
             step_ev[i][0].record()
             wl.step(events=evs[i])
             step_ev[i][1].record()
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    barrier(world)
     launches = csa2.launch_count() - launches0
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    tw0 = time.time()
+    graph.replay()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk.mark(tw0, time.time())
+    clk.stop()
+    barrier(world)
     ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
     ms_max = max_over_ranks(ms, world, dev)
     gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
@@ -432,6 +441,7 @@ def run_csa2(args, world, rank, local):
         if cfg.steps > 1 and wl.step_i >= cfg.steps:
             wl.reset_positions()
 
+    clk = ClockSampler(local).start()
     for _ in range(args.warmup):
         maybe_wrap()
         wl.step()
@@ -439,29 +449,44 @@ def run_csa2(args, world, rank, local):
     if cfg.steps > 1:
         wl.reset_positions()
 
+    # The timed region is ONE CUDA graph holding all K steps (host launch
+    # overhead removed): per step an L2 flush, then [start event, step with
+    # its phase events, end event]. Events are external graph nodes.
     # per-group events: [0] scan start, [1] scan end, [2] after Top-K/pool, then one per layer
     def mk():
-        e = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True, external=True)
         e.record()
         return e
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
     grp_ev = [[[mk() for _ in range(3 + 1 + cfg.groups[g][1])] for g in range(G)] for _ in range(args.steps)]
     torch.cuda.synchronize()
+    if cfg.steps > 1:
+        wl.reset_positions()
+        wl.step_i = 1                                   # captured steps advance the positions
     launches0 = csa2.launch_count()
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
         for i in range(args.steps):
-            maybe_wrap()
-            flush.zero_()                                  # evict L2 between steps (outside the step events)
+            flush.zero_()                              # evict L2 between steps (outside the step events)
             step_ev[i][0].record()
             wl.step(events=grp_ev[i])
             step_ev[i][1].record()
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    launches = csa2.launch_count() - launches0        # kernels launched per replay of the timed graph
+    if cfg.steps > 1:
+        wl.reset_positions()
+        wl.pos.sub_(1)                                 # the first captured step adds 1
+        wl.n.sub_(1)
+    torch.cuda.synchronize()
     barrier(world)
-    launches = csa2.launch_count() - launches0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    tw0 = time.time()
+    graph.replay()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk.mark(tw0, time.time())
+    clk.stop()
+    barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, dev)

@@ -43,6 +43,7 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
                 cudaStream_t s);
 int topk_init_attributes();
 int prefill_init_attributes();
+int attn_tc_init_attributes();
 int launch_prefill_index(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys, float* scores,
                          int64_t stride, int32_t* st, cudaStream_t s);
 int attn_init_attributes();
@@ -70,6 +71,7 @@ static int ensure_init() {
   int rc = topk_init_attributes();
   if (rc == CSA2_OK) rc = attn_init_attributes();
   if (rc == CSA2_OK) rc = prefill_init_attributes();
+  if (rc == CSA2_OK) rc = attn_tc_init_attributes();
   if (rc == CSA2_OK) done_mask |= (1ull << dev);
   return rc;
 }
@@ -95,9 +97,15 @@ static size_t ws_form_pool(int B, int64_t n_max) {
 
 static bool topk_k_ok(int k) { return k >= 1 && k <= kMaxTopK; }
 
+// Records a caller's timing event; inside a stream capture it becomes an
+// event-record node of the graph (external record), so replays time too.
 static int rec(cudaEvent_t e, cudaStream_t s) {
   if (e == nullptr) return CSA2_OK;
-  return cudaEventRecord(e, s) == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return CSA2_ERR_CUDA;
+  const cudaError_t r = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(e, s, cudaEventRecordExternal)
+                                                            : cudaEventRecord(e, s);
+  return r == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
 // Full indexer: zero the Top-K header, scan with the fused histogram, select.

@@ -152,8 +152,12 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(
     const int sub = warp & 3;
     for (int i = 0; i < nt; ++i) {
       const int acc = i & 1;
-      if (!tc::mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1)) { report(st, CSA2_ERR_TIMEOUT); *s_abort = 1; break; }
-      if (*s_abort) break;
+      // warp-uniform decision: the TMEM loads below are warp-collective
+      const bool got = tc::mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1);
+      if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *s_abort != 0)) {
+        if (lane == 0) { report(st, CSA2_ERR_TIMEOUT); *s_abort = 1; }
+        break;
+      }
       tc::tc_fence_after();
       const int64_t key = (t0 + i) * kPM + sub * 32 + lane;
       const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + acc * kPN;

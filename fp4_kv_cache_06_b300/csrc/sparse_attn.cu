@@ -24,6 +24,8 @@
 //   O += PV : P rounded to bf16 in smem, V by ldmatrix.trans.
 // With more than one split the CTA writes (m, l, unnormalised O) partials and
 // a merge kernel combines them by log-sum-exp.
+#include <stdlib.h>
+
 #include "common.cuh"
 
 namespace csa2 {
@@ -311,11 +313,15 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
 // ---- host ------------------------------------------------------------------
 static int attn_occupancy(int MT) { return MT <= 2 ? 2 : 1; }
 
-// Split count minimising (waves x tiles per split); ties go to fewer splits.
+// Split-K count. A batch that fills the machine runs unsplit (a split writes
+// an fp32 partial of H x 512 per CTA and needs the merge pass). Otherwise
+// minimise waves x tiles per split plus one tile-equivalent for the merge;
+// ties go to fewer splits.
 int attn_splits(int B, int H, int k, int W) {
   const int n_tiles = (k + W + kTile - 1) / kTile;
   const int MT = H / 16;
   const int64_t slots = (int64_t)kSMs * attn_occupancy(MT);
+  if ((int64_t)B >= slots) return 1;
   int best = 1;
   int64_t best_cost = -1;
   for (int s = 1; s <= n_tiles; ++s) {
@@ -323,14 +329,15 @@ int attn_splits(int B, int H, int k, int W) {
     const int sp = (n_tiles + tps - 1) / tps;  // splits actually holding tiles
     if (sp != s) continue;
     const int64_t waves = ((int64_t)B * s + slots - 1) / slots;
-    const int64_t cost = waves * tps;
+    const int64_t cost = waves * tps + (s > 1 ? 1 : 0);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
   }
   return best;
 }
 
 size_t attn_ws_bytes(int B, int H, int k, int W) {
-  const int s = attn_splits(B, H, k, W);
+  const int s1 = attn_splits(B, H, k, W), s2 = attn_splits(B, 64, k, W);
+  const int s = s1 > s2 ? s1 : s2;
   if (s <= 1) return 0;
   const size_t po = (size_t)B * s * H * kD * 4;
   return ((po + 255) & ~(size_t)255) + (size_t)B * s * H * 2 * 4;
@@ -377,11 +384,47 @@ int attn_init_attributes() {
   return CSA2_OK;
 }
 
+int launch_sparse_attn_tc(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                          int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
+                          int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
+                          void* out, float* part_o, float* part_ml, int splits, int tps, int32_t* st,
+                          cudaStream_t s);
+
+// tcgen05 path: all H <= 64 heads of a sequence per CTA, one CTA per SM.
+static int launch_attn_tc_split(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                                int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
+                                int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len,
+                                float softmax_scale, void* out, void* ws, int32_t* st, cudaStream_t s) {
+  const int splits = attn_splits(B, 64, k, W);
+  const int n_tiles = (k + W + kTile - 1) / kTile;
+  const int tps = (n_tiles + splits - 1) / splits;
+  float* part_o = nullptr;
+  float* part_ml = nullptr;
+  if (splits > 1) {
+    part_o = static_cast<float*>(ws);
+    const size_t po = (size_t)B * splits * H * kD * 4;
+    part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + ((po + 255) & ~(size_t)255));
+  }
+  int rc = launch_sparse_attn_tc(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
+                                 swa_tail, swa_len, softmax_scale, out, part_o, part_ml, splits, tps, st, s);
+  if (rc != CSA2_OK || splits == 1) return rc;
+  k_attn_merge<<<(unsigned)(B * H), 128, 0, s>>>(part_o, part_ml, H, splits, reinterpret_cast<__nv_bfloat16*>(out));
+  count_launch();
+  return launch_status();
+}
+
 int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
                        int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
                        void* out, void* ws, int32_t* st, cudaStream_t s) {
   if (B == 0) return CSA2_OK;
+  static const bool use_mma_sync = [] {
+    const char* e = getenv("CSA2_ATTN_MMA_SYNC");
+    return e != nullptr && e[0] == '1';
+  }();
+  if (!use_mma_sync)
+    return launch_attn_tc_split(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
+                                swa_tail, swa_len, softmax_scale, out, ws, st, s);
   switch (H) {
     case 16: return launch_attn_mt<1>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_tail, swa_len, softmax_scale, out, ws, st, s);
     case 32: return launch_attn_mt<2>(q, B, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W, swa_tail, swa_len, softmax_scale, out, ws, st, s);

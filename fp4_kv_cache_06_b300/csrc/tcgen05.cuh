@@ -33,12 +33,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete, giving up after
-// `limit` polls (each try_wait may itself suspend for a short while). Returns
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase with the given parity to complete. try_wait may
+// suspend the thread for a while on each poll, so the bound is on wall time
+// (2 s, read from %globaltimer) as well as on the number of polls. Returns
 // false on timeout; the caller reports CSA2_ERR_TIMEOUT and winds down.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = (1u << 22)) {
-  for (uint32_t i = 0; i < limit; ++i)
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && globaltimer_ns() - t0 > 2000000000ull) return false;
+  }
   return false;
 }
 
@@ -105,6 +114,7 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt
          ((M >> 4) << 24);
 }
 constexpr uint32_t kFmtE4M3 = 0;   // kind::f8f6f4
+constexpr uint32_t kFmtF16 = 0;    // kind::f16
 constexpr uint32_t kFmtBF16 = 1;   // kind::f16
 
 // ---- MMA (one thread issues) -------------------------------------------------------

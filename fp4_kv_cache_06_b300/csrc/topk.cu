@@ -99,27 +99,45 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_compact(const float* __rest
   const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
   uint64_t* out = cand + (int64_t)b * kCandCap;
   const int lane = threadIdx.x & 31;
-  for (int64_t i0 = c0; i0 < c1; i0 += kTkThreads) {
-    const int64_t i = i0 + threadIdx.x;
-    bool take = false;
-    uint64_t key = 0;
-    if (i < c1) {
-      const int32_t p = cp ? cp[i] : (int32_t)i;
-      const float v = s[i];
-      if (p >= 0 && (int)(score_key(v) >> 20) >= vbin) {
-        take = true;
-        key = cand_key(v, p);
+  // each thread owns 8 consecutive candidates per pass, read up front (vector
+  // loads when the row is 16-byte aligned) so their latencies overlap
+  const bool vec = ((reinterpret_cast<uintptr_t>(s) | (cp ? reinterpret_cast<uintptr_t>(cp) : 0)) & 15) == 0 &&
+                   (c0 & 7) == 0;
+  for (int64_t i0 = c0; i0 < c1; i0 += (int64_t)kTkThreads * 8) {
+    const int64_t i = i0 + (int64_t)threadIdx.x * 8;
+    float v[8];
+    int32_t p[8];
+    if (vec && i + 8 <= c1) {
+      const float4 a = *reinterpret_cast<const float4*>(s + i), bq = *reinterpret_cast<const float4*>(s + i + 4);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = bq.x; v[5] = bq.y; v[6] = bq.z; v[7] = bq.w;
+      if (cp) {
+        const int4 pa = *reinterpret_cast<const int4*>(cp + i), pb = *reinterpret_cast<const int4*>(cp + i + 4);
+        p[0] = pa.x; p[1] = pa.y; p[2] = pa.z; p[3] = pa.w; p[4] = pb.x; p[5] = pb.y; p[6] = pb.z; p[7] = pb.w;
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) p[u] = (int32_t)(i + u);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool in = i + u < c1;
+        v[u] = in ? s[i + u] : 0.f;
+        p[u] = in ? (cp ? cp[i + u] : (int32_t)(i + u)) : -1;
       }
     }
-    const uint32_t m = __ballot_sync(0xffffffffu, take);
-    if (m) {
-      uint32_t basei = 0;
-      const int leader = __ffs(m) - 1;
-      if (lane == leader) basei = atomicAdd(&hdr[b].cnt, (uint32_t)__popc(m));
-      basei = __shfl_sync(0xffffffffu, basei, leader);
-      if (take) {
-        const uint32_t slot = basei + __popc(m & ((1u << lane) - 1u));
-        if (slot < (uint32_t)kCandCap) out[slot] = key;  // always true: the row did not overflow
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool take = p[u] >= 0 && (int)(score_key(v[u]) >> 20) >= vbin;
+      const uint32_t m = __ballot_sync(0xffffffffu, take);
+      if (m) {
+        uint32_t basei = 0;
+        const int leader = __ffs(m) - 1;
+        if (lane == leader) basei = atomicAdd(&hdr[b].cnt, (uint32_t)__popc(m));
+        basei = __shfl_sync(0xffffffffu, basei, leader);
+        if (take) {
+          const uint32_t slot = basei + __popc(m & ((1u << lane) - 1u));
+          if (slot < (uint32_t)kCandCap) out[slot] = cand_key(v[u], p[u]);   // always: the row did not overflow
+        }
       }
     }
   }
@@ -154,10 +172,33 @@ template <class Src>
 __device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
   __shared__ uint64_t s_prefix;
   __shared__ int s_remaining;
+  __shared__ unsigned long long s_and, s_or;
   const int tid = threadIdx.x;
-  uint64_t prefix = 0, mask = 0;
+  // bits shared by every key are fixed: skip the digits above the first difference
+  if (tid == 0) { s_and = ~0ull; s_or = 0ull; }
+  __syncthreads();
+  {
+    unsigned long long a = ~0ull, o = 0ull;
+    const int64_t m = src.size();
+    for (int64_t i = tid; i < m; i += kFinThreads) {
+      uint64_t key;
+      if (src.get(i, key)) { a &= key; o |= key; }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      a &= __shfl_xor_sync(0xffffffffu, a, off);
+      o |= __shfl_xor_sync(0xffffffffu, o, off);
+    }
+    if ((tid & 31) == 0) { atomicAnd(&s_and, a); atomicOr(&s_or, o); }
+  }
+  __syncthreads();
+  const uint64_t diff = s_and ^ s_or;                 // bits that are not common to all keys
+  const int top = diff ? 63 - __clzll((long long)diff) : -1;
+  int start = 56;
+  while (start > 0 && start > top) start -= 8;        // first digit holding a differing bit
+  uint64_t mask = start < 56 ? ~((1ull << (start + 8)) - 1) : 0ull;
+  uint64_t prefix = s_and & mask;
   int remaining = k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
+  for (int shift = start; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kFinThreads) h256[i] = 0;
     __syncthreads();
     const int64_t m = src.size();
@@ -229,9 +270,6 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
   uint64_t thr = 0;
   if (n_keys > k) thr = radix_kth(src, k, h256);
   if (tid == 0) s_cnt = 0;
-  int np = 1;
-  while (np < k) np <<= 1;
-  for (int i = tid; i < np; i += kFinThreads) sel[i] = 0x7FFFFFFF;
   __syncthreads();
   const int64_t m = src.size();
   const int lane = tid & 31;
@@ -252,8 +290,23 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
   }
   __syncthreads();
   const int cnt = (int)min(s_cnt, (uint32_t)k);
-  bitonic_sort_i32(sel, np);
-  for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? sel[i] : -1;
+  if (k <= 512) {
+    // ascending order by rank: the chosen positions are distinct, so the rank
+    // of one is the number of chosen positions below it (reads broadcast)
+    for (int i = tid; i < cnt; i += kFinThreads) {
+      const int32_t mine = sel[i];
+      int rank = 0;
+      for (int j = 0; j < cnt; ++j) rank += sel[j] < mine;
+      out[rank] = mine;
+    }
+    for (int i = cnt + tid; i < k; i += kFinThreads) out[i] = -1;
+  } else {
+    int np = 1;
+    while (np < k) np <<= 1;
+    for (int i = cnt + tid; i < np; i += kFinThreads) sel[i] = 0x7FFFFFFF;
+    bitonic_sort_i32(sel, np);
+    for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? sel[i] : -1;
+  }
 }
 
 __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restrict__ scores,

@@ -240,11 +240,13 @@ CSA2_API int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t
 /* ---- a7+a8+a9: sparse attention over FP4 rows + SWA [CSA2][CED][FP4] --- */
 /* out[b][h] = softmax(scale * q[b][h] . X^T) X over the keys X = the
  * dequantised main-KV rows idx[b][0..k) (-1 = absent; main K = V) followed
- * by the first swa_len[b] rows of the sequence's SWA block (K = V, bf16).
- * Dequantisation (E2M1 x E4M3) is exact in bf16; Q.K^T and P.V run on the
- * tensor cores in bf16 with fp32 accumulation; the sparse and SWA parts are
- * computed as split-K partials and merged by log-sum-exp. A row with no key
- * at all gets zeros.
+ * by the present rows of the sequence's SWA window (K = V, bf16).
+ * Q.K^T and P.V run on the tcgen05 tensor cores with fp16 operands and fp32
+ * accumulation (TMEM): the FP4 dequantisation (E2M1 x E4M3) is exact in
+ * fp16, Q and SWA rows are converted from bf16 (exact for magnitudes
+ * 2^-14 .. 65504, 2^-24 absolute below, saturating above), probabilities
+ * are rounded to fp16. Key tiles beyond one CTA are split-K partials merged
+ * by log-sum-exp. A row with no key at all gets zeros.
  *   q, out   [B][H][d] bf16
  *   codes/scales row (b,t) at (b*kv_seq_stride + t); t must be < n_cap
  *            (checked: CSA2_ERR_DEVICE_BOUNDS, key skipped)

@@ -57,14 +57,20 @@ def vmax_of(keys):
 
 
 def check_attn(gpu_out, oracle_out, max_abs=ATTN_MAX_ABS, mean_abs=ATTN_MEAN_ABS, vmax=None):
+    """max-abs / mean-abs parity of bf16 outputs against float64. The max-abs
+    bound applies on top of the output format's own rounding: a bf16 output
+    cannot be closer to the exact value than half an ulp (2^-9 |ref|), which
+    alone reaches 2e-3 at |ref| ~ 0.5."""
     g = bf16_to_f64(gpu_out)
     r = np.asarray(oracle_out)
     d = np.abs(g - r)
     assert np.all(np.isfinite(g))
-    extra = 0.0 if vmax is None else BF16_REL * (np.asarray(vmax) + np.abs(r))
-    bound = max_abs + extra
-    worst = np.argmax(d - bound)
-    assert np.all(d <= bound), f"abs err {d.flat[worst]:.3e} > bound {np.broadcast_to(bound, d.shape).flat[worst]:.3e} (max err {d.max():.3e})"
+    extra = 0.0 if vmax is None else BF16_REL * np.asarray(vmax)
+    bound = max_abs + BF16_REL * np.abs(r) + extra
+    worst = np.argmax(d - np.broadcast_to(bound, d.shape))
+    assert np.all(d <= bound), (f"abs err {d.flat[worst]:.3e} > bound {np.broadcast_to(bound, d.shape).flat[worst]:.3e} "
+                                f"at |ref| {abs(r.flat[worst]):.4f} (gpu {g.flat[worst]:.6f}, max err {d.max():.3e}, "
+                                f"mean err {d.mean():.3e}, max |ref| {np.abs(r).max():.3f})")
     mbound = mean_abs + (0.0 if vmax is None else float(np.mean(extra)))
     assert d.mean() <= mbound, f"mean abs err {d.mean():.3e} > {mbound:.3e}"
     return float(d.max()), float(d.mean())
