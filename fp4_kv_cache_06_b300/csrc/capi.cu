@@ -43,10 +43,10 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
                 cudaStream_t s);
 int topk_init_attributes();
 int prefill_init_attributes();
+int scan_init_attributes();
 int attn_tc_init_attributes();
 int launch_prefill_index(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys, float* scores,
                          int64_t stride, int32_t* st, cudaStream_t s);
-int attn_init_attributes();
 int attn_splits(int B, int H, int k, int W);
 size_t attn_ws_bytes(int B, int H, int k, int W);
 int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
@@ -69,8 +69,8 @@ static int ensure_init() {
   std::lock_guard<std::mutex> lk(mu);
   if (done_mask & (1ull << dev)) return CSA2_OK;
   int rc = topk_init_attributes();
-  if (rc == CSA2_OK) rc = attn_init_attributes();
   if (rc == CSA2_OK) rc = prefill_init_attributes();
+  if (rc == CSA2_OK) rc = scan_init_attributes();
   if (rc == CSA2_OK) rc = attn_tc_init_attributes();
   if (rc == CSA2_OK) done_mask |= (1ull << dev);
   return rc;
@@ -277,6 +277,8 @@ int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int6
   if (!index_dims_ok(H_I, d_I)) return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (B == 0 || n_max == 0) return CSA2_OK;
   if (!qI || !w || !kI || !n || !scores || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
+  const int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
   return launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, scores_stride,
                            nullptr, 0, nullptr, nullptr, nullptr, 0, d_status, static_cast<cudaStream_t>(stream));
 }

@@ -53,35 +53,48 @@ constexpr int kTkThreads = 256;
 
 // Threshold bin of a 4096-bin histogram (counted from the top): the highest
 // bin v with (keys in bins >= v) >= k, or bin 0 when the row holds fewer than
-// k keys; *out_ge = keys in bins >= v. Needs all kTkThreads threads.
+// k keys; *out_ge = keys in bins >= v. Every thread of the block must call it
+// (it synchronises); the first kTkThreads threads do the work.
 __device__ __forceinline__ void find_threshold_bin(const uint32_t* __restrict__ h, int k, int* out_bin,
                                                    uint32_t* out_ge) {
-  __shared__ uint32_t part[kTkThreads];
+  __shared__ uint32_t warp_tot[kTkThreads / 32];
   __shared__ int s_bin;
   __shared__ uint32_t s_ge;
-  const int tid = threadIdx.x;
-  const int hi = kHistBins - 16 * tid;  // this thread's bins [hi-16, hi)
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const bool act = tid < kTkThreads;
+  const int hi = kHistBins - 16 * tid;  // this thread's bins [hi-16, hi), counted from the top
   uint32_t loc = 0;
+  if (act) {
 #pragma unroll
-  for (int i = 1; i <= 16; ++i) loc += h[hi - i];
-  part[tid] = loc;
+    for (int i = 1; i <= 16; ++i) loc += h[hi - i];
+  }
+  uint32_t incl = loc;                   // inclusive scan inside the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (act && lane == 31) warp_tot[wid] = incl;
   if (tid == 0) { s_bin = 0; s_ge = 0xFFFFFFFFu; }
   __syncthreads();
-  for (int off = 1; off < kTkThreads; off <<= 1) {   // inclusive scan over threads
-    const uint32_t v = tid >= off ? part[tid - off] : 0;
-    __syncthreads();
-    part[tid] += v;
-    __syncthreads();
-  }
-  const uint32_t incl = part[tid], excl = incl - loc;
-  const uint32_t total = part[kTkThreads - 1];
-  if (total < (uint32_t)k) {
-    if (tid == 0) { s_bin = 0; s_ge = total; }
-  } else if (excl < (uint32_t)k && incl >= (uint32_t)k) {
-    uint32_t run = excl;
-    for (int i = 1; i <= 16; ++i) {
-      run += h[hi - i];
-      if (run >= (uint32_t)k) { s_bin = hi - i; s_ge = run; break; }
+  if (act) {
+    uint32_t before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kTkThreads / 32; ++w) {
+      const uint32_t x = warp_tot[w];
+      before += w < wid ? x : 0u;
+      total += x;
+    }
+    incl += before;
+    const uint32_t excl = incl - loc;
+    if (total < (uint32_t)k) {
+      if (tid == 0) { s_bin = 0; s_ge = total; }
+    } else if (excl < (uint32_t)k && incl >= (uint32_t)k) {
+      uint32_t run = excl;
+      for (int i = 1; i <= 16; ++i) {
+        run += h[hi - i];
+        if (run >= (uint32_t)k) { s_bin = hi - i; s_ge = run; break; }
+      }
     }
   }
   __syncthreads();
@@ -89,15 +102,15 @@ __device__ __forceinline__ void find_threshold_bin(const uint32_t* __restrict__ 
   *out_ge = s_ge;
 }
 
-// End of a histogram-producing CTA (kTkThreads threads): add the CTA's
-// shared histogram into the row's global one; the last CTA of the row to
-// finish (counted with an atomic, no waiting) derives the threshold bin and
-// the overflow flag for the compaction step. `sh` is reused as scratch.
+// End of a histogram-producing CTA: add the CTA's shared histogram into the
+// row's global one; the last CTA of the row to finish (counted with an
+// atomic, no waiting) derives the threshold bin and the overflow flag for
+// the compaction step. `sh` is reused as scratch. Every thread calls it.
 __device__ __forceinline__ void topk_hist_flush(uint32_t* sh, uint32_t* __restrict__ ghist, TopkHdr* hdr,
                                                 int k, unsigned ctas_in_row) {
   __shared__ int s_last;
   __syncthreads();
-  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) {
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
     const uint32_t v = sh[i];
     if (v) atomicAdd(ghist + i, v);
   }
@@ -107,7 +120,7 @@ __device__ __forceinline__ void topk_hist_flush(uint32_t* sh, uint32_t* __restri
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = __ldcg(ghist + i);
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = __ldcg(ghist + i);
   __syncthreads();
   int vbin;
   uint32_t ge;

@@ -23,6 +23,7 @@
 // (12 high bits of the order-preserving score key) is accumulated in shared
 // memory and flushed once per CTA.
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace csa2 {
 
@@ -138,6 +139,136 @@ __global__ void __launch_bounds__(kScanThreads) k_index_scan(
   if (hist) topk_hist_flush(sh_hist, hist + (int64_t)b * kHistBins, hdr + b, topk_k, gridDim.x);
 }
 
+// ---- TMA-staged variant for contiguous rows of 128-byte keys ------------------
+// The big Full-layer and pool-formation scans stream 16 KB tiles (128 rows x
+// 128 B) through a 5-stage shared-memory ring with TMA (128-byte swizzle);
+// one producer warp issues the copies, 8 consumer warps each take one
+// 16-row m-tile of every tile. Bytes in flight are then set by the ring, not
+// by registers. Inside an m-tile, fragment row g reads smem row sigma(g) =
+// {0,4,1,5,2,6,3,7}[g] (and +8): with the swizzle this makes every 16-byte
+// shared load of a quarter-warp hit 8 distinct bank groups.
+constexpr int kTmaStages = 5;
+constexpr int kTmaRows = 128;
+constexpr int kTmaTile = kTmaRows * 128;          // 16 KB
+constexpr int kTmaThreads = 288;                  // 8 consumer warps + 1 producer warp
+constexpr int kTmaSmem = kTmaStages * kTmaTile + 1024 + 64;
+
+__global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
+    const __grid_constant__ CUtensorMap map_k, const uint8_t* __restrict__ qI, const float* __restrict__ w,
+    int64_t kI_seq_stride, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max, int tiles_per_cta,
+    float* __restrict__ scores, int64_t scores_stride, uint32_t* __restrict__ hist, TopkHdr* __restrict__ hdr,
+    int topk_k, int32_t* st) {
+  __shared__ uint32_t sh_hist[kHistBins];
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023) & ~1023u;
+  unsigned char* sp = smem_raw + (base - raw);
+  const uint32_t bar_full = base + kTmaStages * kTmaTile, bar_empty = bar_full + 8 * kTmaStages;
+  const int b = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+
+  int64_t nb = n[b];
+  nb = nb < 0 ? nb : (nb + len_div - 1) / len_div;
+  if (nb > n_max || nb < 0) {
+    if (blockIdx.x == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+    nb = nb < 0 ? 0 : n_max;
+  }
+  const int64_t tiles_b = (nb + kTmaRows - 1) / kTmaRows;
+  const int64_t t0 = (int64_t)blockIdx.x * tiles_per_cta;
+  const int64_t t1 = min(t0 + (int64_t)tiles_per_cta, tiles_b);
+  const int nt = t1 > t0 ? (int)(t1 - t0) : 0;
+
+  if (hist)
+    for (int i = tid; i < kHistBins; i += kTmaThreads) sh_hist[i] = 0;
+  if (tid == 0) {
+    for (int i = 0; i < kTmaStages; ++i) {
+      tc::mbar_init(bar_full + 8 * i, 1);
+      tc::mbar_init(bar_empty + 8 * i, 8);
+    }
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 8) {
+    if (lane == 0 && nt > 0) {                     // producer
+      tc::prefetch_tmap(&map_k);
+      for (int i = 0; i < nt; ++i) {
+        const int s = i % kTmaStages;
+        if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kTmaStages) & 1) ^ 1)) { report(st, CSA2_ERR_TIMEOUT); break; }
+        tc::mbar_expect_tx(bar_full + 8 * s, kTmaTile);
+        tc::tma_load_2d(base + s * kTmaTile, &map_k, 0,
+                        (int32_t)((int64_t)b * kI_seq_stride + (t0 + i) * kTmaRows), bar_full + 8 * s);
+      }
+    }
+  } else {                                         // consumers: warp w owns m-tile w of every tile
+    uint32_t qf[8];
+    {
+      const bool live = g < H_I;
+      const uint8_t* qrow = qI + ((int64_t)b * H_I + (live ? g : 0)) * 128;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + 64 * c + 16 * t) : make_uint4(0, 0, 0, 0);
+        qf[4 * c + 0] = v.x; qf[4 * c + 1] = v.y; qf[4 * c + 2] = v.z; qf[4 * c + 3] = v.w;
+      }
+    }
+    const float w0 = (2 * t < H_I) ? w[(int64_t)b * H_I + 2 * t] : 0.f;
+    const float w1 = (2 * t + 1 < H_I) ? w[(int64_t)b * H_I + 2 * t + 1] : 0.f;
+    float* srow = scores + (int64_t)b * scores_stride;
+    const int sg = ((g & 1) << 2) | (g >> 1);       // sigma(g)
+    const int r1 = warp * 16 + sg, r2 = r1 + 8;     // tile rows of fragment rows g and g+8
+    for (int i = 0; i < nt; ++i) {
+      const int s = i % kTmaStages;
+      const bool got = tc::mbar_wait(bar_full + 8 * s, (i / kTmaStages) & 1);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) report(st, CSA2_ERR_TIMEOUT);
+        break;
+      }
+      const unsigned char* tile = sp + s * kTmaTile;
+      uint4 a[2][2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        a[0][c] = *reinterpret_cast<const uint4*>(tile + r1 * 128 + (((4 * c + t) ^ (r1 & 7)) << 4));
+        a[1][c] = *reinterpret_cast<const uint4*>(tile + r2 * 128 + (((4 * c + t) ^ (r2 & 7)) << 4));
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4& x0 = a[0][j >> 1];
+        const uint4& x1 = a[1][j >> 1];
+        mma_e4m3_16832(acc, (j & 1) ? x0.z : x0.x, (j & 1) ? x1.z : x1.x, (j & 1) ? x0.w : x0.y,
+                       (j & 1) ? x1.w : x1.y, qf[2 * j], qf[2 * j + 1]);
+      }
+      float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
+      float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      if (t < 2) {
+        const int64_t row = (t0 + i) * kTmaRows + (t ? r2 : r1);
+        const float sc = t ? s1 : s0;
+        if (row < nb) {
+          srow[row] = sc;
+          if (hist) atomicAdd(&sh_hist[score_key(sc) >> 20], 1u);
+        }
+      }
+    }
+  }
+  if (hist) topk_hist_flush(sh_hist, hist + (int64_t)b * kHistBins, hdr + b, topk_k, gridDim.x);
+}
+
+bool make_tmap_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows);
+
+static int tma_scan_init = 0;
+int scan_init_attributes() {
+  if (cudaFuncSetAttribute(k_index_scan_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  tma_scan_init = 1;
+  return CSA2_OK;
+}
+
 // rows_per_cta: a multiple of the CTA's rows per iteration, sized so the
 // grid covers the machine a few times over.
 static int64_t scan_rows_per_cta(int B, int64_t rows) {
@@ -154,6 +285,26 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
   const bool use_pool = pool != nullptr;
   const int64_t rows = use_pool ? (int64_t)P * kBlock : n_max;
   if (rows == 0 || B == 0) return CSA2_OK;
+  if (!use_pool && d_I == 128 && tma_scan_init) {
+    // the key rows of all sequences as one 2-D tensor [rows][128 B]
+    const uint64_t total_rows = (uint64_t)(B - 1) * (uint64_t)kI_seq_stride + (uint64_t)n_max;
+    CUtensorMap map;
+    if (make_tmap_rows128(&map, kI, total_rows, 128, kTmaRows)) {
+      const int64_t tiles = (n_max + kTmaRows - 1) / kTmaRows;
+      // one wave of two CTAs per SM: each CTA streams a long contiguous run of
+      // tiles, so the ring is filled once per CTA
+      int64_t per_seq = (2 * kSMs) / B;
+      if (per_seq > tiles) per_seq = tiles;
+      if (per_seq < 1) per_seq = 1;
+      const int tpc = (int)((tiles + per_seq - 1) / per_seq);
+      per_seq = (tiles + tpc - 1) / tpc;
+      dim3 grid((unsigned)per_seq, (unsigned)B);
+      k_index_scan_tma<<<grid, kTmaThreads, kTmaSmem, s>>>(map, qI, w, kI_seq_stride, n, len_div, H_I, n_max, tpc,
+                                                           scores, scores_stride, hist, hdr, topk_k, st);
+      count_launch();
+      return launch_status();
+    }
+  }
   const int64_t per = scan_rows_per_cta(B, rows);
   dim3 grid((unsigned)((rows + per - 1) / per), (unsigned)B);
 #define CSA2_SCAN(DI_, POOL_)                                                                   \
