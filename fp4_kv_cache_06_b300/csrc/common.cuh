@@ -10,6 +10,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -23,6 +25,42 @@ constexpr int kBlock = 8;              // positions per pool block
 // ---- host bookkeeping ------------------------------------------------------
 void count_launch();
 int launch_status();                   // CSA2_OK or CSA2_ERR_CUDA after a launch
+// After a launch that returned `e`: also clears the runtime's last error.
+inline int launch_status(cudaError_t e) {
+  const int st = launch_status();
+  return e == cudaSuccess ? st : CSA2_ERR_CUDA;
+}
+
+// ---- programmatic dependent launch -----------------------------------------
+// The kernels of a step are launched with programmatic stream serialization,
+// so a kernel's launch and its prologue overlap the tail of the kernel before
+// it. Every kernel launched this way executes pdl_wait() before its first
+// global-memory access and before any return: the wait blocks until the
+// preceding kernel has completed and its writes are visible (and, since that
+// kernel waited in turn, everything before it), so the stream order holds.
+// Without the launch attribute the wait returns at once. pdl_trigger() lets
+// the next kernel start launching once every CTA of this one has issued it
+// or exited; kernels that allocate TMEM issue it only after their allocation
+// and allocate only after their wait, so a waiting CTA never holds columns
+// that a running one still needs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- device status ---------------------------------------------------------
 __device__ __forceinline__ void report(int32_t* st, int code) {

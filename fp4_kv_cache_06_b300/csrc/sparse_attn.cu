@@ -14,30 +14,60 @@ namespace csa2 {
 constexpr int kD = 512;          // main head dim
 constexpr int kTile = 64;        // keys per tile of the attention kernel
 
-// Log-sum-exp merge of split-K partials: one CTA of 128 threads per (b, h).
+// Log-sum-exp merge of split-K partials. Partial O is stored
+// [b][split][dim / 4][H][4] and (m, l) as [b][split][H][2]; one thread per
+// (four dims, head) with heads fastest, so a warp's loads are contiguous. The
+// kernel is bound by load latency: U splits' loads are all issued before any
+// is used (U >= splits for decode shapes: one round trip), with an online
+// rescale across rounds when there are more splits than U.
+template <int U>
 __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ part_o,
-                                                    const float* __restrict__ part_ml, int H,
-                                                    int splits, __nv_bfloat16* __restrict__ out) {
-  const int bh = blockIdx.x;
-  const int b = bh / H, h = bh - b * H;
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, part_ml[(((int64_t)b * splits + s) * H + h) * 2]);
-  float Lsum = 0.f;
+                                                    const float* __restrict__ part_ml, int H, int splits,
+                                                    __nv_bfloat16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (kD / 4) * H) return;
+  const int d4 = i / H, h = i - d4 * H;
+  const float* ml = part_ml + ((int64_t)b * splits * H + h) * 2;
+  const float* po = part_o + ((int64_t)b * splits * (kD / 4) + d4) * H * 4 + h * 4;
+  const int64_t po_split = (int64_t)(kD / 4) * H * 4;
+  float M = -INFINITY, Lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int dim = threadIdx.x * 4;
-  if (M != -INFINITY) {
-    for (int s = 0; s < splits; ++s) {
-      const int64_t pidx = ((int64_t)b * splits + s) * H + h;
-      const float m = part_ml[pidx * 2], l = part_ml[pidx * 2 + 1];
-      if (m == -INFINITY) continue;
-      const float wgt = exp2f(m - M);
-      Lsum += wgt * l;
-      const float4 v = *reinterpret_cast<const float4*>(part_o + pidx * kD + dim);
-      acc.x += wgt * v.x; acc.y += wgt * v.y; acc.z += wgt * v.z; acc.w += wgt * v.w;
+  for (int s0 = 0; s0 < splits; s0 += U) {
+    float m[U], l[U];
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      m[u] = -INFINITY;
+      l[u] = 0.f;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + u < splits) {
+        const float2 x = *reinterpret_cast<const float2*>(ml + (int64_t)(s0 + u) * H * 2);
+        m[u] = x.x;
+        l[u] = x.y;
+        v[u] = *reinterpret_cast<const float4*>(po + (s0 + u) * po_split);
+      }
     }
+    float Mc = M;
+#pragma unroll
+    for (int u = 0; u < U; ++u) Mc = fmaxf(Mc, m[u]);
+    if (Mc == -INFINITY) continue;                   // nothing attended so far
+    const float sc = exp2f(M - Mc);                  // 0 while M is still -inf
+    Lsum *= sc;
+    acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (m[u] == -INFINITY) continue;
+      const float wgt = exp2f(m[u] - Mc);
+      Lsum += wgt * l[u];
+      acc.x += wgt * v[u].x; acc.y += wgt * v[u].y; acc.z += wgt * v[u].z; acc.w += wgt * v[u].w;
+    }
+    M = Mc;
   }
   const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-  __nv_bfloat16* o = out + ((int64_t)b * H + h) * kD + dim;
+  __nv_bfloat16* o = out + ((int64_t)b * H + h) * kD + 4 * d4;
   *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
 }
@@ -98,9 +128,13 @@ int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const 
   int rc = launch_sparse_attn_tc(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
                                  swa_tail, swa_len, softmax_scale, out, part_o, part_ml, splits, tps, st, s);
   if (rc != CSA2_OK || splits == 1) return rc;
-  k_attn_merge<<<(unsigned)(B * H), 128, 0, s>>>(part_o, part_ml, H, splits, reinterpret_cast<__nv_bfloat16*>(out));
+  const dim3 grid((unsigned)(((kD / 4) * H + 127) / 128), (unsigned)B);
+  auto kern = splits <= 4 ? k_attn_merge<4> : splits <= 8 ? k_attn_merge<8> : k_attn_merge<16>;
+  const cudaError_t e = launch_pdl(kern, grid, dim3(128), 0, s, static_cast<const float*>(part_o),
+                                   static_cast<const float*>(part_ml), H, splits,
+                                   reinterpret_cast<__nv_bfloat16*>(out));
   count_launch();
-  return launch_status();
+  return launch_status(e);
 }
 
 }  // namespace csa2

@@ -30,8 +30,9 @@
 //             lanes 64..127 of the same 256 columns: two MMAs with A = [P; 0]
 //             and A = [0; P] (zero rows leave the other half unchanged).
 // TMEM: S at columns 0..63, O at 256..511 (512 allocated, one CTA per SM).
-// Split-K partials (m, l, unnormalised O) are merged by the existing
-// log-sum-exp merge kernel. Waits on MMA completion are bounded.
+// Split-K partials (m, l, unnormalised O; O stored [dim/4][head][4] so the
+// epilogue's stores and the merge's loads are contiguous across heads) are
+// merged by the log-sum-exp merge kernel. Waits on MMA completion are bounded.
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -111,13 +112,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   const int n_tiles = (k + W + kTT - 1) / kTT;
   const int t_begin = split * tiles_per_split;
   const int t_end = min(t_begin + tiles_per_split, n_tiles);
-  int slen = swa_len[b];
-  if (slen > W || slen < 0) {
-    if (split == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
-    slen = slen < 0 ? 0 : W;
-  }
-
-  // ---- set-up: barriers, TMEM, Q tile, zero block, row sources of the first tile
+  // ---- set-up: barriers and the zero block touch no global memory and overlap
+  //      the preceding kernel; then wait for it, allocate TMEM, load the Q tile
+  //      and the row sources of the first tiles
   if (tid == 0) {
     tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_o, 1);
@@ -125,6 +122,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     sMisc[1] = 0;
     sMisc[2] = 0;
   }
+  for (int e = tid; e < 3 * 8192 / 16; e += kTThreads)      // P, Z, P' zero
+    *reinterpret_cast<uint4*>(sp + L::kP + e * 16) = make_uint4(0, 0, 0, 0);
+  pdl_wait();
   if (warp == 0) {
     tc::tmem_alloc(base + L::kMisc, 512);
     tc::tmem_relinquish();
@@ -133,8 +133,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     const int h = e >> 6, c = e & 63;
     if (h < H) cp_async16_hint(base + L::kKV + kt_off(h, c), q + ((int64_t)b * H + h) * kTD + c * 8, pol_stream);
   }
-  for (int e = tid; e < 3 * 8192 / 16; e += kTThreads)      // P, Z, P' zero
-    *reinterpret_cast<uint4*>(sp + L::kP + e * 16) = make_uint4(0, 0, 0, 0);
+  // the SWA length is clamped without a branch, so nothing waits on its load
+  // before the row-index loads are issued
+  const int slen_in = swa_len[b];
+  const int slen = min(max(slen_in, 0), W);
 
   auto row_sources = [&](int tile, int buf) {
     if (tid < kTT) {
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sMisc[0];
+  pdl_trigger();                              // TMEM is held: the next kernel may start launching
   if (t_begin < t_end) gather_fp4(t_begin % L::kNS);
   cp_async_commit();
   if (t_begin + 1 < t_end) gather_fp4((t_begin + 1) % L::kNS);
@@ -246,20 +249,37 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     // -- dequant FP4 rows, one 16-channel group (one scale) per step: group g
     //    of row r = code bytes 8g..8g+7 -> dims 16g..16g+15 = chunks 2g, 2g+1
     {
+      // thread (warp w, lane g) dequantises group g of rows w, w + 8, .., w + 56;
+      // all eight rows' codes and scales are loaded before any is converted
       const unsigned char* stg = sp + L::kStage + buf * L::kStageBytes;
-      for (int e = tid; e < kTT * 32; e += kTThreads) {
-        const int r = e >> 5, g = e & 31;
-        if (sSrc[buf * kTT + r] < 0 || sKind[buf * kTT + r] != 0) continue;
-        const uint2 cw = *reinterpret_cast<const uint2*>(stg + r * 256 + g * 8);
-        uint32_t sh2;                                           // scale as f16x2 {s, s}
-        {
-          const uint16_t sb = stg[kTT * 256 + r * 32 + g];
-          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sh2) : "h"((uint16_t)(sb | (sb << 8))));
+      const uint32_t* vmask = reinterpret_cast<const uint32_t*>(sp + L::kMask) + buf * 2;
+      const uint32_t* smask = reinterpret_cast<const uint32_t*>(sp + L::kMask + 32) + buf * 2;
+      const uint64_t fp4rows = ((uint64_t)vmask[0] | ((uint64_t)vmask[1] << 32)) &
+                               ~((uint64_t)smask[0] | ((uint64_t)smask[1] << 32));
+      constexpr int kRowsPerThread = kTT * 32 / kTThreads;
+      const int g = lane;
+      uint2 cw[kRowsPerThread];
+      uint32_t sb[kRowsPerThread];
+#pragma unroll
+      for (int it = 0; it < kRowsPerThread; ++it) {
+        const int r = warp + 8 * it;
+        cw[it] = make_uint2(0u, 0u);
+        sb[it] = 0u;
+        if ((fp4rows >> r) & 1) {
+          cw[it] = *reinterpret_cast<const uint2*>(stg + r * 256 + g * 8);
+          sb[it] = stg[kTT * 256 + r * 32 + g];
         }
+      }
+#pragma unroll
+      for (int it = 0; it < kRowsPerThread; ++it) {
+        const int r = warp + 8 * it;
+        if (!((fp4rows >> r) & 1)) continue;
+        uint32_t sh2;                                           // scale as f16x2 {s, s}
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sh2) : "h"((uint16_t)(sb[it] | (sb[it] << 8))));
         uint32_t o[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint32_t byte = ((u < 4 ? cw.x : cw.y) >> (8 * (u & 3))) & 0xFF;
+          const uint32_t byte = ((u < 4 ? cw[it].x : cw[it].y) >> (8 * (u & 3))) & 0xFF;
           const uint32_t h2 = e2m1x2_to_f16x2(byte);
           asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[u]) : "r"(h2), "r"(sh2));
         }
@@ -369,6 +389,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     if (__syncthreads_or(!ok)) break;          // uniform exit after a timed-out wait
   }
   cp_async_wait<0>();
+  if ((slen_in < 0 || slen_in > W) && split == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
   // ---- epilogue
   if (n_pv > 0) {
     if (!tc::mbar_wait(bar_o, (n_pv - 1) & 1)) report(st, CSA2_ERR_TIMEOUT);
@@ -377,28 +398,35 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   if (!ok) n_pv = 0;                          // a timed-out CTA writes zeros
   if (tid < 64) { sL[tid] = l_run; sMx[tid] = m_run; }
   __syncthreads();
-  if (warp < 4) {
-    // whole warps read TMEM (tcgen05.ld is warp-collective); lanes of heads >= H only skip the stores
-    const int h = (32 * warp + lane) & 63, half = warp >> 1;
+  {
+    // All eight warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (row r holds
+    // head r % 64, dims 0..255 for r < 64 and 256..511 above) and the column
+    // half w / 4 of O's 256 columns. tcgen05.ld is warp-collective, so whole
+    // warps load; lanes of heads >= H only skip the stores.
+    const int lg = warp & 3, chalf = warp >> 2;
+    const int row = 32 * lg + lane, h = row & 63;
     const bool live = h < H;
-    const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + kTOcol;
+    const uint32_t ta = tmem + ((uint32_t)(32 * lg) << 16) + kTOcol + 128 * chalf;
     const float lsum = sL[h];
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    for (int c = 0; c < 256; c += 32) {
-      uint32_t r[32];
+    const int dbase = (row >> 6) * 256 + 128 * chalf;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 64) {
+      uint32_t r[64];
       if (n_pv > 0) {
         tc::tmem_ld32(ta + c, r);
+        tc::tmem_ld32(ta + c + 32, r + 32);
         tc::tmem_ld_wait();
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = 0u;
+        for (int j = 0; j < 64; ++j) r[j] = 0u;
       }
       if (!live) continue;
-      const int dim0 = half * 256 + c;
+      const int dim0 = dbase + c;
       if (splits == 1) {
         __nv_bfloat16* o = out + ((int64_t)b * H + h) * kTD + dim0;
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
+        for (int j = 0; j < 64; j += 8) {
           uint32_t pk[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -409,14 +437,16 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
           st_global_hint(o + j, make_uint4(pk[0], pk[1], pk[2], pk[3]), pol_stream);
         }
       } else {
-        float* o = part_o + (((int64_t)b * splits + split) * H + h) * kTD + dim0;
+        // partial O layout [b][split][dim / 4][H][4]: a warp stores 32 heads' float4 contiguously
+        float* o = part_o + ((((int64_t)b * splits + split) * (kTD / 4) + dim0 / 4) * H + h) * 4;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(o + j) = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        for (int j = 0; j < 64; j += 4)
+          *reinterpret_cast<float4*>(o + (int64_t)(j / 4) * H * 4) =
+              make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]), __uint_as_float(r[j + 2]),
+                          __uint_as_float(r[j + 3]));
       }
     }
-    if (live && splits > 1 && half == 0) {
+    if (live && splits > 1 && row < 64 && chalf == 0) {
       const int64_t pidx = ((int64_t)b * splits + split) * H + h;
       part_ml[pidx * 2 + 0] = sMx[h];
       part_ml[pidx * 2 + 1] = sL[h];
@@ -443,12 +473,13 @@ int launch_sparse_attn_tc(const void* q, int B, int H, const uint8_t* codes, con
                           void* out, float* part_o, float* part_ml, int splits, int tps, int32_t* st,
                           cudaStream_t s) {
   dim3 grid((unsigned)splits, (unsigned)B);
-  k_sparse_attn_tc<<<grid, kTThreads, TcSmem::kBytes, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(q), H, codes, scales, kv_seq_stride, n_cap, idx, k,
-      reinterpret_cast<const __nv_bfloat16*>(swa), swa_seq_stride, W, swa_tail, swa_len,
-      softmax_scale * 1.4426950408889634f, splits, tps, reinterpret_cast<__nv_bfloat16*>(out), part_o, part_ml, st);
+  const cudaError_t e = launch_pdl(
+      k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, reinterpret_cast<const __nv_bfloat16*>(q), H,
+      codes, scales, kv_seq_stride, n_cap, idx, k, reinterpret_cast<const __nv_bfloat16*>(swa), swa_seq_stride, W,
+      swa_tail, swa_len, softmax_scale * 1.4426950408889634f, splits, tps, reinterpret_cast<__nv_bfloat16*>(out),
+      part_o, part_ml, st);
   count_launch();
-  return launch_status();
+  return launch_status(e);
 }
 
 }  // namespace csa2

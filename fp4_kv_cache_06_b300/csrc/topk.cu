@@ -10,33 +10,47 @@
 // k best are exactly the k largest keys and the result does not depend on
 // the order in which threads or CTAs visit the candidates.
 //
-// Pipeline per row (three launches; the first is fused into the indexer
-// scan when the scan runs just before):
-//   1. histogram of the 12 high key bits (4096 bins) over the row;
-//   2. compaction: every CTA derives the same threshold bin from the
-//      histogram and appends the candidates at or above it (at most
-//      kCandCap) to the row's candidate buffer; if more than kCandCap would
-//      qualify the row is flagged and left to step 3's slow path;
-//   3. one CTA per row: exact radix select of the k-th largest key over the
-//      compacted candidates in shared memory (or, for a flagged row, over the
-//      whole row in global memory), then a bitonic sort of the chosen
-//      positions, -1 padding.
+// Pipeline per row:
+//   1. histogram of the 12 high score-key bits (4096 bins) over the row,
+//      fused into the indexer scan when the scan runs just before; the last
+//      CTA of the row finds the threshold bin (the one holding the k-th
+//      largest score) and flags the row if more than kCandCap entries lie at
+//      or above it;
+//   2. rows longer than kDirectRows: ordered compaction. The row is cut into
+//      chunks of kChunk entries; a CTA compacts a chunk (the entries at or
+//      above the threshold bin, in index order), reserves room for it with a
+//      single atomic and records (base, count) in the row's chunk table;
+//   3. one CTA per row gathers the candidates in index order (through the
+//      chunk table, or straight from the row when it is short). When the
+//      positions increase with the index (position-indexed rows, pool slots)
+//      the k-th score is resolved inside the threshold bin by two 10-bit
+//      histogram passes, ties at that score go to the first entries in index
+//      order (the smallest positions), and the chosen entries are written in
+//      index order, which is ascending position order: no sort. Otherwise,
+//      and for flagged rows (over the whole row in global memory), an exact
+//      radix select over the 64-bit keys is followed by a sort.
 #include "common.cuh"
 
 namespace csa2 {
 
 
+constexpr int kChunk = kTkThreads * 8;        // entries per compaction chunk
+constexpr int kMaxChunks = 4096;              // chunk-table entries per row (rows up to 8M entries)
+constexpr int64_t kDirectRows = 32768;        // rows this short skip step 2
+
 // Workspace layout (all offsets 256-byte aligned):
-//   hist [B][kHistBins] u32 | hdr [B] TopkHdr | cand [B][kCandCap] u64
+//   hist [B][kHistBins] u32 | hdr [B] TopkHdr | cand [B][kCandCap] u64 |
+//   tab [B][kMaxChunks] {base, count}
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t topk_ws_bytes(int B) {
   return align256((size_t)B * kHistBins * 4) + align256((size_t)B * sizeof(TopkHdr)) +
-         align256((size_t)B * kCandCap * 8);
+         align256((size_t)B * kCandCap * 8) + align256((size_t)B * kMaxChunks * 8);
 }
 struct TopkWs {
   uint32_t* hist;
   TopkHdr* hdr;
   uint64_t* cand;
+  uint2* tab;
 };
 static TopkWs topk_ws(void* ws, int B) {
   char* p = static_cast<char*>(ws);
@@ -46,6 +60,8 @@ static TopkWs topk_ws(void* ws, int B) {
   r.hdr = reinterpret_cast<TopkHdr*>(p);
   p += align256((size_t)B * sizeof(TopkHdr));
   r.cand = reinterpret_cast<uint64_t*>(p);
+  p += align256((size_t)B * kCandCap * 8);
+  r.tab = reinterpret_cast<uint2*>(p);
   return r;
 }
 uint32_t* topk_ws_hist(void* ws) { return static_cast<uint32_t*>(ws); }
@@ -61,6 +77,59 @@ __device__ __forceinline__ int64_t row_len(const int64_t* n, int b, int len_div,
   return v < n_max ? v : n_max;
 }
 
+// Exclusive prefix sum of one value per thread over a CTA of NT threads;
+// *total receives the CTA's sum. s_warp holds NT / 32 words. Contains two
+// barriers, so every thread of the CTA must call it.
+template <int NT>
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* s_warp, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  if (lane == 31) s_warp[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    const uint32_t x = s_warp[w];
+    before += w < wid ? x : 0u;
+    tot += x;
+  }
+  __syncthreads();
+  *total = tot;
+  return before + incl - v;
+}
+
+// Eight consecutive entries i..i+7 of a row (fewer at its end): score and
+// position (-1 = absent), with vector loads when the whole group is inside the
+// row and 16-byte aligned.
+__device__ __forceinline__ void load8(const float* __restrict__ s, const int32_t* __restrict__ cp, int64_t i,
+                                      int64_t len, float* v, int32_t* p) {
+  const bool vec = i + 8 <= len &&
+                   ((reinterpret_cast<uintptr_t>(s + i) | (cp ? reinterpret_cast<uintptr_t>(cp + i) : 0)) & 15) == 0;
+  if (vec) {
+    const float4 a = *reinterpret_cast<const float4*>(s + i), c = *reinterpret_cast<const float4*>(s + i + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    if (cp) {
+      const int4 pa = *reinterpret_cast<const int4*>(cp + i), pb = *reinterpret_cast<const int4*>(cp + i + 4);
+      p[0] = pa.x; p[1] = pa.y; p[2] = pa.z; p[3] = pa.w; p[4] = pb.x; p[5] = pb.y; p[6] = pb.z; p[7] = pb.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) p[u] = (int32_t)(i + u);
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = i + u < len;
+      v[u] = in ? s[i + u] : 0.f;
+      p[u] = in ? (cp ? cp[i + u] : (int32_t)(i + u)) : -1;
+    }
+  }
+}
+
 // ---- step 1 (standalone form) --------------------------------------------
 __global__ void __launch_bounds__(kTkThreads) k_topk_hist(const float* __restrict__ scores,
                                                           const int32_t* __restrict__ cand_pos,
@@ -71,6 +140,8 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_hist(const float* __restric
   __shared__ uint32_t sh[kHistBins];
   const int b = blockIdx.y;
   for (int i = threadIdx.x; i < kHistBins; i += kTkThreads) sh[i] = 0;
+  pdl_trigger();
+  pdl_wait();
   __syncthreads();
   const int64_t nb = row_len(n, b, len_div, n_max);
   const int64_t c0 = (int64_t)blockIdx.x * per, c1 = min(c0 + per, nb);
@@ -84,61 +155,50 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_hist(const float* __restric
 }
 
 // ---- step 2 ----------------------------------------------------------------
+// Ordered compaction of rows longer than kDirectRows: chunk c of row b holds
+// entries [c * kChunk, (c + 1) * kChunk); thread t owns eight consecutive
+// entries of it. The chunk's candidates land contiguously, in index order, at
+// a base reserved by one atomic, and tab[b][c] = (base, count).
 __global__ void __launch_bounds__(kTkThreads) k_topk_compact(const float* __restrict__ scores,
                                                              const int32_t* __restrict__ cand_pos,
                                                              int64_t stride, const int64_t* __restrict__ n,
-                                                             int len_div, int64_t n_max, int64_t per,
+                                                             int len_div, int64_t n_max,
                                                              TopkHdr* __restrict__ hdr,
-                                                             uint64_t* __restrict__ cand) {
+                                                             uint64_t* __restrict__ cand, uint2* __restrict__ tab) {
+  __shared__ uint32_t s_warp[kTkThreads / 32];
+  __shared__ uint32_t s_base;
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y;
   if (hdr[b].overflow) return;
   const int vbin = hdr[b].vbin;
   const int64_t nb = row_len(n, b, len_div, n_max);
-  const int64_t c0 = (int64_t)blockIdx.x * per, c1 = min(c0 + per, nb);
+  const int64_t nch = (nb + kChunk - 1) / kChunk;
   const float* s = scores + (int64_t)b * stride;
   const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
   uint64_t* out = cand + (int64_t)b * kCandCap;
-  const int lane = threadIdx.x & 31;
-  // each thread owns 8 consecutive candidates per pass, read up front (vector
-  // loads when the row is 16-byte aligned) so their latencies overlap
-  const bool vec = ((reinterpret_cast<uintptr_t>(s) | (cp ? reinterpret_cast<uintptr_t>(cp) : 0)) & 15) == 0 &&
-                   (c0 & 7) == 0;
-  for (int64_t i0 = c0; i0 < c1; i0 += (int64_t)kTkThreads * 8) {
-    const int64_t i = i0 + (int64_t)threadIdx.x * 8;
+  for (int64_t ch = blockIdx.x; ch < nch; ch += gridDim.x) {
+    const int64_t i = ch * kChunk + (int64_t)threadIdx.x * 8;
     float v[8];
     int32_t p[8];
-    if (vec && i + 8 <= c1) {
-      const float4 a = *reinterpret_cast<const float4*>(s + i), bq = *reinterpret_cast<const float4*>(s + i + 4);
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = bq.x; v[5] = bq.y; v[6] = bq.z; v[7] = bq.w;
-      if (cp) {
-        const int4 pa = *reinterpret_cast<const int4*>(cp + i), pb = *reinterpret_cast<const int4*>(cp + i + 4);
-        p[0] = pa.x; p[1] = pa.y; p[2] = pa.z; p[3] = pa.w; p[4] = pb.x; p[5] = pb.y; p[6] = pb.z; p[7] = pb.w;
-      } else {
+    load8(s, cp, i, nb, v, p);
+    uint32_t take = 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) p[u] = (int32_t)(i + u);
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = i + u < c1;
-        v[u] = in ? s[i + u] : 0.f;
-        p[u] = in ? (cp ? cp[i + u] : (int32_t)(i + u)) : -1;
-      }
+    for (int u = 0; u < 8; ++u)
+      if (p[u] >= 0 && (int)(score_key(v[u]) >> 20) >= vbin) take |= 1u << u;
+    uint32_t tot;
+    const uint32_t excl = block_excl_scan<kTkThreads>(__popc(take), s_warp, &tot);
+    if (threadIdx.x == 0) {
+      s_base = tot ? atomicAdd(&hdr[b].cnt, tot) : 0u;
+      if (ch < kMaxChunks) tab[(int64_t)b * kMaxChunks + ch] = make_uint2(s_base, tot);
     }
+    __syncthreads();
+    uint32_t slot = s_base + excl;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const bool take = p[u] >= 0 && (int)(score_key(v[u]) >> 20) >= vbin;
-      const uint32_t m = __ballot_sync(0xffffffffu, take);
-      if (m) {
-        uint32_t basei = 0;
-        const int leader = __ffs(m) - 1;
-        if (lane == leader) basei = atomicAdd(&hdr[b].cnt, (uint32_t)__popc(m));
-        basei = __shfl_sync(0xffffffffu, basei, leader);
-        if (take) {
-          const uint32_t slot = basei + __popc(m & ((1u << lane) - 1u));
-          if (slot < (uint32_t)kCandCap) out[slot] = cand_key(v[u], p[u]);   // always: the row did not overflow
-        }
-      }
+      if (!((take >> u) & 1)) continue;
+      if (slot < (uint32_t)kCandCap) out[slot] = cand_key(v[u], p[u]);   // always: the row did not overflow
+      ++slot;
     }
   }
 }
@@ -309,43 +369,218 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
   }
 }
 
+// Digit d of a 1024-bin histogram (one bin per thread) at which the count
+// taken from the top reaches `need` (> 0, at most the histogram's sum):
+// *digit = d and *above = the count of entries in bins above d.
+__device__ void find_digit_from_top(const uint32_t* h, uint32_t need, uint32_t* s_warp, int* digit,
+                                    uint32_t* above) {
+  __shared__ int s_digit;
+  __shared__ uint32_t s_above;
+  const int d = kFinThreads - 1 - threadIdx.x;
+  const uint32_t c = h[d];
+  if (threadIdx.x == 0) { s_digit = 0; s_above = 0; }   // defined result even for an inconsistent histogram
+  uint32_t tot;
+  const uint32_t excl = block_excl_scan<kFinThreads>(c, s_warp, &tot);   // entries in bins above d
+  if (excl < need && excl + c >= need) { s_digit = d; s_above = excl; }
+  __syncthreads();
+  *digit = s_digit;
+  *above = s_above;
+  __syncthreads();
+}
+
+// Candidates keys[0..cnt) in index order with increasing positions, all at or
+// above threshold bin vbin: write the k best positions, ascending, to out.
+__device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, int32_t* __restrict__ out,
+                               uint32_t* h, uint32_t* s_warp) {
+  const int tid = threadIdx.x;
+  if (cnt <= k) {
+    for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? cand_pos_of(keys[i]) : -1;
+    return;
+  }
+  // entries above the threshold bin are all taken
+  uint32_t above = 0;
+  for (int i = tid; i < cnt; i += kFinThreads) above += (int)(keys[i] >> 52) > vbin;
+  uint32_t c_above;
+  block_excl_scan<kFinThreads>(above, s_warp, &c_above);
+  uint32_t need = (uint32_t)k - c_above;              // >= 1: the k-th score lies in the bin
+  // score-key bits 19..10 of the entries in the threshold bin
+  h[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < cnt; i += kFinThreads) {
+    const uint64_t key = keys[i];
+    if ((int)(key >> 52) == vbin) atomicAdd(&h[(key >> 42) & 1023], 1u);
+  }
+  __syncthreads();
+  int dA, dB;
+  uint32_t aA, aB;
+  find_digit_from_top(h, need, s_warp, &dA, &aA);
+  need -= aA;
+  const uint64_t preA = ((uint64_t)vbin << 10) | (uint64_t)dA;   // score key >> 10
+  // score-key bits 9..0 of the entries sharing that prefix
+  h[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < cnt; i += kFinThreads) {
+    const uint64_t key = keys[i];
+    if ((key >> 42) == preA) atomicAdd(&h[(key >> 32) & 1023], 1u);
+  }
+  __syncthreads();
+  find_digit_from_top(h, need, s_warp, &dB, &aB);
+  const uint32_t r = need - aB;                        // entries to take at exactly the k-th score
+  const uint32_t thr = (uint32_t)((preA << 10) | (uint64_t)dB);
+  // ordered output: thread t owns entries [lo, hi); ties at thr go to the
+  // first r in index order
+  const int S = (cnt + kFinThreads - 1) / kFinThreads;
+  const int lo = min(tid * S, cnt), hi = min(lo + S, cnt);
+  uint32_t ties = 0;
+  for (int i = lo; i < hi; ++i) ties += (uint32_t)(keys[i] >> 32) == thr;
+  uint32_t tot;
+  const uint32_t tie0 = block_excl_scan<kFinThreads>(ties, s_warp, &tot);
+  uint32_t takes = 0, tr = tie0;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t sk = (uint32_t)(keys[i] >> 32);
+    if (sk > thr) ++takes;
+    else if (sk == thr) takes += (tr++ < r) ? 1u : 0u;
+  }
+  uint32_t o = block_excl_scan<kFinThreads>(takes, s_warp, &tot);   // tot == k
+  tr = tie0;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t sk = (uint32_t)(keys[i] >> 32);
+    bool take = sk > thr;
+    if (sk == thr) take = tr++ < r;
+    if (take && o < (uint32_t)k) out[o++] = cand_pos_of(keys[i]);
+  }
+}
+
+// Gather modes of step 3.
+enum FinalMode : int { kFinDirect = 0, kFinTable = 1, kFinUnordered = 2 };
+
 __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restrict__ scores,
                                                             const int32_t* __restrict__ cand_pos,
                                                             int64_t stride, const int64_t* __restrict__ n,
                                                             int len_div, int64_t n_max, int k,
                                                             const TopkHdr* __restrict__ hdr,
                                                             const uint64_t* __restrict__ cand,
+                                                            const uint2* __restrict__ tab, int mode,
                                                             int32_t* __restrict__ idx_out) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint64_t* keys = reinterpret_cast<uint64_t*>(smem);                 // kCandCap
-  uint32_t* h256 = reinterpret_cast<uint32_t*>(keys + kCandCap);      // 256
-  int32_t* sel = reinterpret_cast<int32_t*>(h256 + 256);              // kMaxTopK
-  const int b = blockIdx.x;
+  uint32_t* h = reinterpret_cast<uint32_t*>(keys + kCandCap);         // 1024 (256 for the radix select)
+  int32_t* sel = reinterpret_cast<int32_t*>(h + 1024);                // kMaxTopK
+  uint32_t* pre = reinterpret_cast<uint32_t*>(sel + kMaxTopK);        // kMaxChunks
+  uint32_t* cbase = pre + kMaxChunks;                                 // kMaxChunks
+  __shared__ uint32_t s_warp[kFinThreads / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, tid = threadIdx.x;
   int32_t* out = idx_out + (int64_t)b * k;
   const int64_t nb = row_len(n, b, len_div, n_max);
+  const float* s = scores + (int64_t)b * stride;
+  const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
   if (hdr[b].overflow) {
     // slow path: count the row's present candidates, then select over global memory
     __shared__ uint32_t s_valid;
-    if (threadIdx.x == 0) s_valid = 0;
+    if (tid == 0) s_valid = 0;
     __syncthreads();
-    const float* s = scores + (int64_t)b * stride;
-    const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
     uint32_t loc = 0;
-    for (int64_t i = threadIdx.x; i < nb; i += kFinThreads) loc += (cp == nullptr || cp[i] >= 0);
+    for (int64_t i = tid; i < nb; i += kFinThreads) loc += (cp == nullptr || cp[i] >= 0);
     atomicAdd(&s_valid, loc);
     __syncthreads();
     RowKeys src{s, cp, nb};
-    select_and_write(src, k, (int64_t)s_valid, out, h256, sel);
+    select_and_write(src, k, (int64_t)s_valid, out, h, sel);
     return;
   }
-  const int cnt = (int)min(hdr[b].cnt, (uint32_t)kCandCap);
-  for (int i = threadIdx.x; i < cnt; i += kFinThreads) keys[i] = cand[(int64_t)b * kCandCap + i];
+  const int vbin = hdr[b].vbin;
+  int cnt = 0;
+  if (mode == kFinDirect) {
+    // the row itself, in index order: entries at or above the threshold bin
+    uint32_t run = 0;
+    for (int64_t i0 = 0; i0 < nb; i0 += (int64_t)kFinThreads * 8) {
+      const int64_t i = i0 + (int64_t)tid * 8;
+      float v[8];
+      int32_t p[8];
+      load8(s, cp, i, nb, v, p);
+      uint32_t take = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (p[u] >= 0 && (int)(score_key(v[u]) >> 20) >= vbin) take |= 1u << u;
+      uint32_t tot;
+      uint32_t slot = run + block_excl_scan<kFinThreads>(__popc(take), s_warp, &tot);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (!((take >> u) & 1)) continue;
+        if (slot < (uint32_t)kCandCap) keys[slot] = cand_key(v[u], p[u]);
+        ++slot;
+      }
+      run += tot;
+    }
+    cnt = (int)min(run, (uint32_t)kCandCap);
+  } else if (mode == kFinTable) {
+    // chunk order is index order: prefix of the chunk counts, then one
+    // binary search per candidate into the prefix
+    const int nch = (int)((nb + kChunk - 1) / kChunk);
+    constexpr int kPer = kMaxChunks / kFinThreads;
+    uint2 e[kPer];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = tid * kPer + u;
+      e[u] = c < nch ? tab[(int64_t)b * kMaxChunks + c] : make_uint2(0u, 0u);
+      sum += e[u].y;
+    }
+    uint32_t tot;
+    uint32_t run = block_excl_scan<kFinThreads>(sum, s_warp, &tot);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = tid * kPer + u;
+      if (c < nch) { pre[c] = run; cbase[c] = e[u].x; }
+      run += e[u].y;
+    }
+    __syncthreads();
+    cnt = (int)min(tot, (uint32_t)kCandCap);
+    const uint64_t* rc = cand + (int64_t)b * kCandCap;
+    constexpr int kG = kCandCap / kFinThreads;
+    uint64_t kv[kG];
+#pragma unroll
+    for (int u = 0; u < kG; ++u) {
+      const int o = tid + u * kFinThreads;
+      kv[u] = 0;
+      if (o < cnt) {
+        int lo = 0, hi = nch - 1;                     // last chunk with pre <= o
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (pre[mid] <= (uint32_t)o) lo = mid; else hi = mid - 1;
+        }
+        const uint32_t slot = cbase[lo] + ((uint32_t)o - pre[lo]);
+        kv[u] = rc[slot < (uint32_t)kCandCap ? slot : 0];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kG; ++u) {
+      const int o = tid + u * kFinThreads;
+      if (o < cnt) keys[o] = kv[u];
+    }
+  } else {
+    cnt = (int)min(hdr[b].cnt, (uint32_t)kCandCap);
+    for (int i = tid; i < cnt; i += kFinThreads) keys[i] = cand[(int64_t)b * kCandCap + i];
+  }
   __syncthreads();
-  SmemKeys src{keys, cnt};
-  select_and_write(src, k, cnt, out, h256, sel);
+  // positions increasing along the candidates: select in order, no sort
+  bool mono = mode != kFinUnordered;
+  if (mono) {
+    const int S = (cnt + kFinThreads - 1) / kFinThreads;
+    const int lo = min(tid * S, cnt), hi = min(lo + S + 1, cnt);
+    for (int i = lo + 1; i < hi; ++i)
+      if (cand_pos_of(keys[i - 1]) >= cand_pos_of(keys[i])) mono = false;
+  }
+  if (__syncthreads_and(mono)) {
+    ordered_select(keys, cnt, vbin, k, out, h, s_warp);
+  } else {
+    SmemKeys src{keys, cnt};
+    select_and_write(src, k, cnt, out, h, sel);
+  }
 }
 
-int topk_final_smem() { return kCandCap * 8 + 256 * 4 + kMaxTopK * 4; }
+int topk_final_smem() { return kCandCap * 8 + 1024 * 4 + kMaxTopK * 4 + 2 * kMaxChunks * 4; }
 
 // ---- host ------------------------------------------------------------------
 static int64_t tk_rows_per_cta(int B, int64_t rows) {
@@ -368,22 +603,33 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
   if (B == 0) return CSA2_OK;
   TopkWs w = topk_ws(ws, B);
   int rc;
-  const int64_t per = tk_rows_per_cta(B, n_max);
-  dim3 grid((unsigned)((n_max + per - 1) / per > 0 ? (n_max + per - 1) / per : 1), (unsigned)B);
   if (!hist_ready) {
     if ((rc = topk_prepare(ws, B, s)) != CSA2_OK) return rc;
-    k_topk_hist<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, w.hist, w.hdr, k);
+    const int64_t per = tk_rows_per_cta(B, n_max);
+    dim3 grid((unsigned)((n_max + per - 1) / per > 0 ? (n_max + per - 1) / per : 1), (unsigned)B);
+    const cudaError_t e = launch_pdl(k_topk_hist, grid, dim3(kTkThreads), 0, s, scores, cand_pos, stride, n, len_div,
+                                     n_max, per, w.hist, w.hdr, k);
     count_launch();
-    if ((rc = launch_status()) != CSA2_OK) return rc;
+    if ((rc = launch_status(e)) != CSA2_OK) return rc;
   }
-  k_topk_compact<<<grid, kTkThreads, 0, s>>>(scores, cand_pos, stride, n, len_div, n_max, per, w.hdr,
-                                             w.cand);
+  const int mode = n_max <= kDirectRows ? kFinDirect
+                   : n_max <= (int64_t)kMaxChunks * kChunk ? kFinTable : kFinUnordered;
+  if (mode != kFinDirect) {
+    const int64_t nch = (n_max + kChunk - 1) / kChunk;
+    int64_t per_row = (4 * kSMs + B - 1) / B;
+    if (per_row > nch) per_row = nch;
+    if (per_row < 1) per_row = 1;
+    const cudaError_t e = launch_pdl(k_topk_compact, dim3((unsigned)per_row, (unsigned)B), dim3(kTkThreads), 0, s,
+                                     scores, cand_pos, stride, n, len_div, n_max, w.hdr, w.cand, w.tab);
+    count_launch();
+    if ((rc = launch_status(e)) != CSA2_OK) return rc;
+  }
+  const cudaError_t e = launch_pdl(k_topk_final, dim3((unsigned)B), dim3(kFinThreads), (size_t)topk_final_smem(), s,
+                                   scores, cand_pos, stride, n, len_div, n_max, k,
+                                   static_cast<const TopkHdr*>(w.hdr), static_cast<const uint64_t*>(w.cand),
+                                   static_cast<const uint2*>(w.tab), mode, idx_out);
   count_launch();
-  if ((rc = launch_status()) != CSA2_OK) return rc;
-  k_topk_final<<<B, kFinThreads, topk_final_smem(), s>>>(scores, cand_pos, stride, n, len_div, n_max, k, w.hdr,
-                                                          w.cand, idx_out);
-  count_launch();
-  return launch_status();
+  return launch_status(e);
 }
 
 int topk_init_attributes() {

@@ -13,7 +13,7 @@
 // until the process exits. Nothing is allocated per call.
 //
 // The array holds the scratch of csa2_topk for at most
-// CSA2_TOPK_NOALLOC_MAX_ROWS rows (about 5.25 MB). All calls share it and it
+// CSA2_TOPK_NOALLOC_MAX_ROWS rows (about 7.25 MB). All calls share it and it
 // keeps whatever the last call left there; each call clears the part that
 // must start at zero (the histograms and row headers) before use. Calls that
 // overlap on the GPU — on two streams, or from two host threads without
@@ -31,9 +31,10 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
                 cudaStream_t s);
 
 // Scratch of csa2_topk for CSA2_TOPK_NOALLOC_MAX_ROWS rows:
-//   histograms 64 x 4096 x 4 B + row headers 64 x 16 B + candidates 64 x 8192 x 8 B,
+//   histograms 64 x 4096 x 4 B + row headers 64 x 16 B + candidates 64 x 8192 x 8 B
+//   + chunk tables 64 x 4096 x 8 B,
 // each region rounded up to 256 bytes (the layout csa2_topk uses).
-constexpr size_t kNoAllocScratchBytes = 1048576 + 1024 + 4194304;
+constexpr size_t kNoAllocScratchBytes = 1048576 + 1024 + 4194304 + 2097152;
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocScratchBytes];
 
 // Device address of g_topk_scratch on each device, looked up once per device

@@ -188,7 +188,7 @@ CSA2_API int csa2_topk(const float* scores, const int32_t* cand_pos,
  * Same selection, arguments and result as csa2_topk, minus the workspace:
  * the scratch lives in a fixed device array inside the library, reserved on
  * every GPU that loads the library and held until the process exits
- * (about 5.25 MB). Limits: at most CSA2_TOPK_NOALLOC_MAX_ROWS rows (B);
+ * (about 7.25 MB). Limits: at most CSA2_TOPK_NOALLOC_MAX_ROWS rows (B);
  * larger B returns CSA2_ERR_UNSUPPORTED_SHAPE and enqueues nothing.
  * The first call made while a device is current looks up that device's
  * array address (one-time set-up); make that first call before capturing

@@ -92,6 +92,28 @@ def test_topk_candidate_positions_and_absent():
         np.testing.assert_array_equal(idx.cpu().numpy()[b], ref)
 
 
+@pytest.mark.parametrize("m", [40000, 8_400_000])
+def test_topk_long_rows_and_unordered_positions(m):
+    """Rows past the short-row limit go through the ordered compaction; rows
+    past the chunk table's reach (8M entries) and candidates whose positions do
+    not increase with the index take the exact 64-bit select and a sort."""
+    rng = np.random.default_rng(m)
+    k = 512
+    s = rng.standard_normal((1, m)).astype(np.float32)
+    idx = torch.empty((1, k), dtype=torch.int32, device=DEV)
+    ws = _ws(csa2.OP_TOPK, 1, m, k)
+    csa2.csa2_topk(torch.from_numpy(s).to(DEV), None, m, k, idx, ws)
+    torch.cuda.synchronize()
+    ref = oracle.topk_select(s[0].astype(np.float64), np.arange(m), k)
+    np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
+    if m < 10 ** 6:
+        pos = rng.permutation(10 ** 7)[:m].reshape(1, m).astype(np.int32)
+        csa2.csa2_topk(torch.from_numpy(s).to(DEV), None, m, k, idx, ws, cand_pos=torch.from_numpy(pos).to(DEV))
+        torch.cuda.synchronize()
+        ref = oracle.topk_select(s[0].astype(np.float64), pos[0], k)
+        np.testing.assert_array_equal(idx.cpu().numpy()[0], ref)
+
+
 def test_form_pool_and_reindex():
     B, d_I, P, k = 3, 128, 2048, 512
     n_list = [40000, 16384, 3001]
