@@ -438,6 +438,15 @@ def scan_traffic(d_I, positions_per_launch):
         return None
 
 
+def decode_config(cfg, config_index, batch, world):
+    """The `config` object of a decode bench line (both arms print the same one)."""
+    return {"workload": cfg.workload, "config_index": config_index, "batch": batch,
+            "context": cfg.n, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}", "topk": cfg.k,
+            "swa": cfg.W, "groups": [list(g) for g in cfg.groups], "parallelism": f"replicas{world}",
+            "l2": "flushed before every step outside the per-step events (256 MiB write, then a 256 MiB read "
+                  "so the write-backs land in the flush)"}
+
+
 def run_csa2(args, world, rank, local):
     import torch
     import synth
@@ -560,10 +569,7 @@ def run_csa2(args, world, rank, local):
         "metric": METRIC, "value": world * wl.B / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
-        "config": {"workload": cfg.workload, "config_index": args.config, "batch": wl.B,
-                   "context": wl.n_end, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}", "topk": cfg.k,
-                   "swa": cfg.W, "groups": [list(g) for g in cfg.groups], "parallelism": f"replicas{world}",
-                   "l2": "flushed before every step outside the per-step events (256 MiB write, then a 256 MiB read so the write-backs land in the flush)"},
+        "config": decode_config(cfg, args.config, wl.B, world),
         "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
         "phases_ms": phase, "wall_s": wall, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
     }
@@ -659,7 +665,7 @@ def run_reference(args, world, rank):
         "metric": METRIC, "impl": "reference", "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.workload, "config_index": args.config, "batch": 1, "context": cfg.n},
+        "config": decode_config(cfg, args.config, args.batch or cfg.B, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
