@@ -60,7 +60,8 @@ def dist_setup(n_gpus):
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
