@@ -162,12 +162,13 @@ class ClockSampler:
 class DecodeWorkload:
     """Caches, per-layer inputs and the per-step calls of one decode config."""
 
-    def __init__(self, cfg, device, seed=1234, batch=None):
+    def __init__(self, cfg, device, seed=1234, batch=None, pool_rule="mean"):
         import torch
         import synth
         from fp4_kv_cache_06_b300 import csa2
         self.torch, self.csa2 = torch, csa2
         self.cfg = cfg
+        self.pool_rule = pool_rule
         self.dev = device
         B = self.B = batch or cfg.B
         d_I, H_I, H, W, k, P = cfg.d_I, cfg.H_I, cfg.H, cfg.W, cfg.k, cfg.P
@@ -213,6 +214,28 @@ class DecodeWorkload:
         self.step_i = 0
         torch.cuda.synchronize()
 
+    def _rule(self, mode):
+        """Pool rule of a group that forms the pool: a Full group may take the
+        block maxima of its own scores; otherwise the blocks' mean keys."""
+        if self.pool_rule == "max" and mode == "full":
+            return self.csa2.POOL_BLOCK_MAX
+        return self.csa2.POOL_MEAN_KEY
+
+    def pool_recall(self):
+        """Share of the pool-forming Full group's Top-k positions whose block is
+        in the pool it formed (after the last step; None without such a group)."""
+        torch = self.torch
+        for g, (mode, _, form_pool) in enumerate(self.cfg.groups):
+            if mode == "full" and form_pool:
+                idx, pool = self.idx[g].long(), self.pool.long()
+                hits = total = 0
+                for b in range(self.B):                      # membership per sequence
+                    sel = idx[b][idx[b] >= 0]
+                    hits += int(torch.isin(sel // 8, pool[b][pool[b] >= 0]).sum())
+                    total += int(sel.numel())
+                return round(hits / max(1, total), 6)
+        return None
+
     def reset_positions(self):
         """Restart the step sequence (positions back to the first step's)."""
         self.step_i = 0
@@ -235,7 +258,8 @@ class DecodeWorkload:
             csa2.csa2_layer_group(
                 csa2.MODE_FULL if mode == "full" else csa2.MODE_REINDEX, self.n, n_max, self.codes, self.scales,
                 self.kI, self.qI[g], self.w[g], self.idx[g], self.q[l0:l0 + L], self.swa[l0:l0 + L], self.swa_len,
-                self.out[l0:l0 + L], self.ws, kbar=self.kbar, pool=self.pool, form_pool=form_pool,
+                self.out[l0:l0 + L], self.ws, kbar=self.kbar, pool=self.pool,
+                form_pool=self._rule(mode) if form_pool else csa2.POOL_NONE,
                 qI_pool=self.qI_pool if mode == "reindex" else None,
                 w_pool=self.w_pool if mode == "reindex" else None,
                 events=None if events is None else events[g])
@@ -439,9 +463,10 @@ def scan_traffic(d_I, positions_per_launch):
         return None
 
 
-def decode_config(cfg, config_index, batch, world):
+def decode_config(cfg, config_index, batch, world, pool_rule="mean"):
     """The `config` object of a decode bench line (both arms print the same one)."""
-    return {"workload": cfg.workload, "config_index": config_index, "batch": batch,
+    extra = {"pool_rule": "block max of the Full scores"} if pool_rule == "max" else {}
+    return {**extra, "workload": cfg.workload, "config_index": config_index, "batch": batch,
             "context": cfg.n, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}", "topk": cfg.k,
             "swa": cfg.W, "groups": [list(g) for g in cfg.groups], "parallelism": f"replicas{world}",
             "l2": "flushed before every step outside the per-step events (256 MiB write, then a 256 MiB read "
@@ -458,7 +483,7 @@ def run_csa2(args, world, rank, local):
     cfg = synth.get_config(args.config)
     if cfg.prefill_queries:
         raise SystemExit("the prefill configuration is not a decode bench workload")
-    wl = DecodeWorkload(cfg, dev, seed=1234 + 7919 * rank, batch=args.batch)
+    wl = DecodeWorkload(cfg, dev, seed=1234 + 7919 * rank, batch=args.batch, pool_rule=args.pool_rule)
     G = len(cfg.groups)
     flush = L2Flush(dev)
     total_steps = args.warmup + args.steps
@@ -570,10 +595,13 @@ def run_csa2(args, world, rank, local):
         "metric": METRIC, "value": world * wl.B / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
-        "config": decode_config(cfg, args.config, wl.B, world),
+        "config": decode_config(cfg, args.config, wl.B, world, args.pool_rule),
         "roofline": roof, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk.summary(),
         "phases_ms": phase, "wall_s": wall, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
     }
+    recall = wl.pool_recall()
+    if recall is not None:
+        res["pool_recall"] = recall
     return res
 
 
@@ -666,7 +694,7 @@ def run_reference(args, world, rank):
         "metric": METRIC, "impl": "reference", "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": decode_config(cfg, args.config, args.batch or cfg.B, world),
+        "config": decode_config(cfg, args.config, args.batch or cfg.B, world, args.pool_rule),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -680,6 +708,8 @@ def main():
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--batch", type=int, default=None, help="override the batch (profiling runs)")
     ap.add_argument("--impl", default="csa2", choices=["csa2", "reference"])
+    ap.add_argument("--pool-rule", default="mean", choices=["mean", "max"],
+                    help="how a Full group that forms the pool scores blocks: mean key (default) or block max")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

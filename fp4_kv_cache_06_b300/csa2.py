@@ -19,12 +19,15 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 OK = 0
 OP_TOPK, OP_INDEX_FULL, OP_INDEX_REINDEX, OP_FORM_POOL, OP_SPARSE_ATTN, OP_LAYER_GROUP = 1, 2, 3, 4, 5, 6
 OP_PREFILL_GROUP = 7
+OP_FORM_POOL_BLOCK_MAX = 8
+POOL_NONE, POOL_MEAN_KEY, POOL_BLOCK_MAX = 0, 1, 2
 MODE_FULL, MODE_REINDEX = 0, 1
 
 EXPORTS = (
     "csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size",
     "csa2_quantize_kv_fp4", "csa2_append_indexer_k", "csa2_block_means", "csa2_append_swa",
-    "csa2_index_scores", "csa2_topk", "csa2_index_full", "csa2_form_pool", "csa2_index_reindex",
+    "csa2_index_scores", "csa2_topk", "csa2_index_full", "csa2_form_pool", "csa2_form_pool_block_max",
+    "csa2_index_reindex",
     "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_prefill_index_scores",
     "csa2_prefill_group",
 )
@@ -90,6 +93,7 @@ def lib() -> ctypes.CDLL:
     L.csa2_topk.argtypes = [_c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i32, _c_p, _c_p, _c_sz, _c_p]
     L.csa2_index_full.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_p, _c_p, _c_p, _c_sz, _c_p, _c_p]
     L.csa2_form_pool.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_i32, _c_i32, _c_i32, _c_i64, _c_i32, _c_p, _c_p, _c_sz, _c_p, _c_p]
+    L.csa2_form_pool_block_max.argtypes = [_c_p, _c_i64, _c_p, _c_i32, _c_i64, _c_i32, _c_p, _c_p, _c_sz, _c_p]
     L.csa2_index_reindex.argtypes = [_c_p, _c_p, _c_p, _c_i64, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_sz, _c_p, _c_p]
     L.csa2_sparse_attn.argtypes = [_c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i64, _c_i64, _c_p, _c_i32, _c_p, _c_i64, _c_i32, _c_i32, _c_p, _c_f, _c_p, _c_p, _c_sz, _c_p, _c_p]
     L.csa2_layer_group.argtypes = [ctypes.POINTER(GroupArgs), _c_p]
@@ -286,6 +290,18 @@ def csa2_form_pool(qI, w, kbar, n, n_max, P, pool_out, ws, kbar_seq_stride=None,
     _check(rc, "csa2_form_pool")
 
 
+def csa2_form_pool_block_max(scores, n, n_max, P, pool_out, ws, stream=None):
+    """Pool by the max-of-token rule: scores [B][stride] fp32 from a Full scan."""
+    _need(scores, "scores", torch.float32, 2)
+    _need(pool_out, "pool_out", torch.int32, 2)
+    _need(ws, "ws", torch.uint8)
+    _opt(n, "n", torch.int64, 1)
+    B = scores.shape[0]
+    rc = lib().csa2_form_pool_block_max(_ptr(scores), scores.shape[1], _ptr(n), B, int(n_max), int(P),
+                                        _ptr(pool_out), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "csa2_form_pool_block_max")
+
+
 def csa2_index_reindex(qI, w, kI, n, pool, k, idx_out, ws, kI_seq_stride=None, d_status=None, stream=None):
     _need(qI, "qI", torch.uint8, 3)
     _need(w, "w", torch.float32, 2)
@@ -353,7 +369,7 @@ def csa2_layer_group(mode, n, n_max, codes, scales, kI, qI, w, idx, q_layers: Se
     a = GroupArgs()
     a.mode = int(mode)
     a.n_reuse = L - 1
-    a.form_pool = int(bool(form_pool))
+    a.form_pool = int(form_pool)               # False/True -> none/mean-key; or a POOL_* rule
     a.B, a.H, a.d, a.H_I, a.d_I = B, H, d, H_I, d_I
     a.k = idx.shape[1]
     a.W = swa_layers[0].shape[1]

@@ -41,6 +41,9 @@ int topk_prepare(void* ws, int B, cudaStream_t s);
 int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, const int64_t* n,
                 int len_div, int B, int64_t n_max, int k, int32_t* idx_out, void* ws, bool hist_ready,
                 cudaStream_t s);
+size_t pool_block_max_ws_bytes(int B, int64_t n_max);
+int launch_pool_block_max(const float* scores, int64_t stride, const int64_t* n, int B, int64_t n_max, int P,
+                          int32_t* pool_out, void* ws, cudaStream_t s);
 int topk_init_attributes();
 int prefill_init_attributes();
 int scan_init_attributes();
@@ -180,7 +183,7 @@ const char* csa2_status_string(int status) {
   }
 }
 
-int csa2_version(void) { return 100; }
+int csa2_version(void) { return 101; }
 
 uint64_t csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -197,8 +200,10 @@ size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k, int3
       size_t m = align256((size_t)B * (size_t)n_max * 4) + topk_ws_bytes(B);
       return m + attn_ws_bytes(B, H, k, 128);
     }
+    case CSA2_OP_FORM_POOL_BLOCK_MAX: return pool_block_max_ws_bytes(B, n_max);
     case CSA2_OP_LAYER_GROUP: {
-      size_t m = ws_index_full(B, n_max);
+      // the block-max pool reads the Full scores, so its workspace follows them
+      size_t m = ws_index_full(B, n_max) + pool_block_max_ws_bytes(B, n_max);
       const size_t r = ws_reindex(B, P), f = ws_form_pool(B, n_max), a = attn_ws_bytes(B, H, k, 128);
       if (r > m) m = r;
       if (f > m) m = f;
@@ -326,6 +331,18 @@ int csa2_form_pool(const uint8_t* qI, const float* w, const uint8_t* kbar, int64
                       static_cast<cudaStream_t>(stream));
 }
 
+int csa2_form_pool_block_max(const float* scores, int64_t scores_stride, const int64_t* n, int32_t B,
+                             int64_t n_max, int32_t P, int32_t* pool_out, void* ws, size_t ws_bytes, void* stream) {
+  if (B < 0 || n_max < 0 || scores_stride < n_max) return CSA2_ERR_INVALID_ARG;
+  if (!topk_k_ok(P) || n_max > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (!scores || !pool_out) return CSA2_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, pool_block_max_ws_bytes(B, n_max))) return CSA2_ERR_WORKSPACE;
+  int rc = ensure_init();
+  if (rc != CSA2_OK) return rc;
+  return launch_pool_block_max(scores, scores_stride, n, B, n_max, P, pool_out, ws, static_cast<cudaStream_t>(stream));
+}
+
 int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
                        const int64_t* n, const int32_t* pool, int32_t P, int32_t B, int32_t H_I,
                        int32_t d_I, int32_t k, int32_t* idx_out, void* ws, size_t ws_bytes,
@@ -374,8 +391,10 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   if (a->B < 0 || a->n_max < 0 || a->n_max > a->n_cap || a->n_max > 0x7FFFFFFF) return CSA2_ERR_INVALID_ARG;
   if (a->B == 0) return CSA2_OK;
   if (!a->n || !a->codes || !a->scales || !a->kI || !a->qI || !a->w || !a->swa_len) return CSA2_ERR_INVALID_ARG;
+  if (a->form_pool < CSA2_POOL_NONE || a->form_pool > CSA2_POOL_BLOCK_MAX) return CSA2_ERR_INVALID_ARG;
+  if (a->form_pool == CSA2_POOL_BLOCK_MAX && a->mode != CSA2_MODE_FULL) return CSA2_ERR_INVALID_ARG;
   if ((a->form_pool || a->mode == CSA2_MODE_REINDEX) && !a->pool) return CSA2_ERR_INVALID_ARG;
-  if (a->form_pool && !a->kbar) return CSA2_ERR_INVALID_ARG;
+  if (a->form_pool == CSA2_POOL_MEAN_KEY && !a->kbar) return CSA2_ERR_INVALID_ARG;
   if (!index_dims_ok(a->H_I, a->d_I) || !topk_k_ok(a->k) || a->P < 0 || a->P > kMaxTopK ||
       (a->form_pool && a->P < 1) || a->d != 512 || a->W < 0 || a->W > 128 ||
       (a->H != 16 && a->H != 32 && a->H != 48 && a->H != 64))
@@ -394,9 +413,12 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   if (a->mode == CSA2_MODE_FULL) {
     rc = full_indexer(a->qI, a->w, a->kI, a->n_cap, a->n, a->B, a->H_I, a->d_I, a->n_max, a->k, a->idx, nullptr,
                       a->ws, a->d_status, s, group_event(a, 0), group_event(a, 1));
-    if (rc == CSA2_OK && a->form_pool)
+    if (rc == CSA2_OK && a->form_pool == CSA2_POOL_MEAN_KEY)
       rc = pool_indexer(qp, wp, a->kbar, nbc, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
                         a->d_status, s);
+    if (rc == CSA2_OK && a->form_pool == CSA2_POOL_BLOCK_MAX)   // the Full scores are still at ws
+      rc = launch_pool_block_max(static_cast<const float*>(a->ws), a->n_max, a->n, a->B, a->n_max, a->P, a->pool,
+                                 static_cast<char*>(a->ws) + ws_index_full(a->B, a->n_max), s);
   } else {
     if ((rc = rec(group_event(a, 0), s)) != CSA2_OK) return rc;
     if (a->form_pool)

@@ -582,6 +582,29 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
 
 int topk_final_smem() { return kCandCap * 8 + 1024 * 4 + kMaxTopK * 4 + 2 * kMaxChunks * 4; }
 
+// ---- block scores of the max-of-token pool rule -------------------------------
+// bmax[b][j] = the largest score of positions 8 j .. 8 j + 7 below n[b]: a
+// block holding any of the row's Top-k positions scores at least the k-th
+// score, so the best P >= k blocks hold every one of them.
+__global__ void __launch_bounds__(256) k_block_max(const float* __restrict__ scores, int64_t stride,
+                                                   const int64_t* __restrict__ n, int64_t n_max,
+                                                   float* __restrict__ bmax, int64_t nb_max) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.y;
+  const int64_t len = row_len(n, b, 1, n_max);
+  const int64_t nblk = (len + kBlock - 1) / kBlock;
+  const float* s = scores + (int64_t)b * stride;
+  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nblk; j += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t0 = j * kBlock;
+    float m = s[t0];
+#pragma unroll
+    for (int u = 1; u < kBlock; ++u)
+      if (t0 + u < len) m = fmaxf(m, s[t0 + u]);
+    bmax[(int64_t)b * nb_max + j] = m;
+  }
+}
+
 // ---- host ------------------------------------------------------------------
 static int64_t tk_rows_per_cta(int B, int64_t rows) {
   int64_t per = 16384;
@@ -630,6 +653,31 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
                                    static_cast<const uint2*>(w.tab), mode, idx_out);
   count_launch();
   return launch_status(e);
+}
+
+// Pool by the max-of-token rule: block maxima of the scores, then the best
+// P blocks (Top-K with its own histogram pass). ws: bmax [B][nb_max] then a
+// Top-K workspace.
+size_t pool_block_max_ws_bytes(int B, int64_t n_max) {
+  const int64_t nb = (n_max + kBlock - 1) / kBlock;
+  return align256((size_t)B * (size_t)nb * 4) + topk_ws_bytes(B);
+}
+int launch_pool_block_max(const float* scores, int64_t stride, const int64_t* n, int B, int64_t n_max, int P,
+                          int32_t* pool_out, void* ws, cudaStream_t s) {
+  if (B == 0) return CSA2_OK;
+  const int64_t nb = (n_max + kBlock - 1) / kBlock;
+  float* bmax = static_cast<float*>(ws);
+  void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)nb * 4);
+  int64_t gx = (nb + 255) / 256;
+  const int64_t cap = (4 * kSMs + B - 1) / B;
+  if (gx > cap) gx = cap;
+  if (gx < 1) gx = 1;
+  const cudaError_t e = launch_pdl(k_block_max, dim3((unsigned)gx, (unsigned)B), dim3(256), 0, s, scores, stride,
+                                   n, n_max, bmax, nb);
+  count_launch();
+  int rc = launch_status(e);
+  if (rc != CSA2_OK) return rc;
+  return launch_topk(bmax, nullptr, nb, n, kBlock, B, nb, P, pool_out, tk, false, s);
 }
 
 int topk_init_attributes() {

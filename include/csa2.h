@@ -86,7 +86,8 @@ enum csa2_op {
   CSA2_OP_FORM_POOL = 4,     /* csa2_form_pool                             */
   CSA2_OP_SPARSE_ATTN = 5,   /* csa2_sparse_attn (split-K partials)        */
   CSA2_OP_LAYER_GROUP = 6,   /* csa2_layer_group (max of the above)        */
-  CSA2_OP_PREFILL_GROUP = 7  /* csa2_prefill_group: B = queries, n_max = entries */
+  CSA2_OP_PREFILL_GROUP = 7, /* csa2_prefill_group: B = queries, n_max = entries */
+  CSA2_OP_FORM_POOL_BLOCK_MAX = 8 /* csa2_form_pool_block_max (n_max = positions) */
 };
 
 /* Bytes of workspace an op needs for B rows of at most n_max candidates,
@@ -226,6 +227,22 @@ CSA2_API int csa2_form_pool(const uint8_t* qI, const float* w, const uint8_t* kb
                    int32_t* pool_out, void* ws, size_t ws_bytes,
                    int32_t* d_status, void* stream);
 
+/* ---- pool by the max-of-token rule --------------------------------------- */
+/* A variant of the pool with guaranteed recall. The pages give no block
+ * score; this one scores block j with the largest of the Full layer's token
+ * scores over its positions 8j .. 8j+7 below n[b], instead of scoring the
+ * block's mean key. A block holding any of the Full Top-k positions then
+ * scores at least the k-th score, so for P >= k the pool contains every one
+ * of them (the mean-key rule gives no such guarantee: relu is convex).
+ *   scores    [B][scores_stride] fp32 (a Full scan's output, not NaN)
+ *   n, n_max  as in csa2_topk (n = positions; blocks = ceil(n/8))
+ *   pool_out  [B][P] ascending block ids, -1 padded; P <= 2048
+ * Workspace: CSA2_OP_FORM_POOL_BLOCK_MAX. */
+CSA2_API int csa2_form_pool_block_max(const float* scores, int64_t scores_stride,
+                                      const int64_t* n, int32_t B, int64_t n_max,
+                                      int32_t P, int32_t* pool_out, void* ws,
+                                      size_t ws_bytes, void* stream);
+
 /* ---- a5+a6: Reindex layer [CSA2] ---------------------------------------- */
 /* Reindex mode: rescore only the positions of the pool's blocks (pool
  * [B][P] ascending block ids, -1 = empty; positions >= n[b] are absent)
@@ -271,12 +288,16 @@ CSA2_API int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d,
 
 /* ---- a10+a11: one layer group [CSA2][TG] -------------------------------- */
 enum csa2_mode { CSA2_MODE_FULL = 0, CSA2_MODE_REINDEX = 1 };
+enum csa2_pool_rule { CSA2_POOL_NONE = 0, CSA2_POOL_MEAN_KEY = 1, CSA2_POOL_BLOCK_MAX = 2 };
 
 /* Arguments of csa2_layer_group. Pointers are device pointers unless noted. */
 typedef struct csa2_group_args {
   int32_t mode;          /* CSA2_MODE_FULL or CSA2_MODE_REINDEX               */
   int32_t n_reuse;       /* Reuse layers that follow the first layer          */
-  int32_t form_pool;     /* Full only: also form the pool for later groups    */
+  int32_t form_pool;     /* also form the pool for later groups (csa2_pool_rule):
+                            CSA2_POOL_MEAN_KEY scores the blocks' mean keys
+                            with qI_pool (any mode); CSA2_POOL_BLOCK_MAX takes
+                            the block maxima of this Full layer's scores     */
   int32_t B, H, d, H_I, d_I, k, W, P;
   int64_t n_max;         /* host bound on every n[b]                          */
   int64_t n_cap;         /* cache capacity (rows per sequence)                */
@@ -284,7 +305,7 @@ typedef struct csa2_group_args {
   const uint8_t* codes;  /* [B][n_cap][d/2]                                   */
   const uint8_t* scales; /* [B][n_cap][d/16]                                  */
   const uint8_t* kI;     /* [B][n_cap][d_I]                                   */
-  const uint8_t* kbar;   /* [B][ceil(n_cap/8)][d_I] (form_pool only)          */
+  const uint8_t* kbar;   /* [B][ceil(n_cap/8)][d_I] (CSA2_POOL_MEAN_KEY only) */
   const uint8_t* qI;     /* [B][H_I][d_I] the first layer's indexer query     */
   const float* w;        /* [B][H_I]                                          */
   const uint8_t* qI_pool;/* pool-forming query (NULL = qI)                    */

@@ -57,6 +57,7 @@ from .csa2 import (
     topk_select,
     full_topk,
     form_pool,
+    form_pool_block_max,
     pool_positions,
     reindex_topk,
     sparse_attention,

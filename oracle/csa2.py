@@ -142,6 +142,25 @@ def form_pool(q_bytes, w, kbar_bytes, P=2048):
     return topk_select(s, np.arange(nb), P), s
 
 
+def form_pool_block_max(scores, n, P=2048, block=8):
+    """Pool variant with guaranteed recall (a reading beyond the pages).
+
+    [CSA2] lets the Full layer form a pool of up to P blocks of 8 positions
+    but does not say how a block is scored. This variant scores block j by
+    the largest Full-layer score of its positions 8j .. 8j+7 below n, and keeps
+    the best min(P, #blocks) blocks by (score desc, block id asc). Any block
+    holding one of the Full Top-k positions then scores at least the k-th
+    score, so for P >= k the pool holds all of them.
+    scores [>= n] float -> (block ids int32 [P] ascending, -1 padded;
+    block scores float64 [ceil(n/8)]).
+    """
+    n = int(n)
+    s = np.asarray(scores, dtype=np.float64)[:n]
+    nb = (n + block - 1) // block
+    bmax = np.array([s[j * block:min((j + 1) * block, n)].max() for j in range(nb)], dtype=np.float64)
+    return topk_select(bmax, np.arange(nb), P), bmax
+
+
 def pool_positions(pool_blocks, n, block=8):
     """Positions covered by the pool's blocks that are < n, ascending."""
     pb = np.asarray(pool_blocks, dtype=np.int64)

@@ -160,3 +160,50 @@ def test_reindex_on_oracle_pool():
     for b in range(B):
         ref_idx, ref_s, ref_pos = oracle.reindex_topk(u8(qI)[b], w.numpy()[b], u8(kI)[b], pools[b], n_list[b], k)
         check_topk(idx.cpu().numpy()[b], ref_idx, ref_s, ref_pos, k)
+
+
+def test_form_pool_block_max_matches_oracle():
+    """Pool by the max-of-token rule from given scores, ragged rows, P < and >= #blocks."""
+    rng = np.random.default_rng(5)
+    n_list = [131072, 40000, 9000, 15]
+    B, m = len(n_list), max(n_list)
+    s = rng.standard_normal((B, m)).astype(np.float32)
+    s[1, :5000] = np.round(s[1, :5000])            # ties on block maxima
+    n = torch.tensor(n_list, dtype=torch.int64, device=DEV)
+    for P in (2048, 512):
+        pool = torch.empty((B, P), dtype=torch.int32, device=DEV)
+        ws = _ws(csa2.OP_FORM_POOL_BLOCK_MAX, B, m)
+        csa2.csa2_form_pool_block_max(torch.from_numpy(s).to(DEV), n, m, P, pool, ws)
+        torch.cuda.synchronize()
+        gp = pool.cpu().numpy()
+        for b in range(B):
+            ref_pool, ref_bs = oracle.form_pool_block_max(s[b].astype(np.float64), n_list[b], P)
+            check_topk(gp[b], ref_pool, ref_bs, np.arange(ref_bs.size), P)
+
+
+def test_full_group_block_max_pool_holds_every_top_position():
+    """A Full layer forming its pool by the block maxima of its own scores:
+    the pool matches the oracle and contains the block of every Top-512
+    position the layer selected."""
+    B, n, H, P = 2, 150000, 64, 2048
+    kI, qI, w = _inputs(B, n, 8, 128, seed=31, bias=0.05)
+    codes = torch.zeros((B, n, 256), dtype=torch.uint8, device=DEV)
+    scales = torch.zeros((B, n, 32), dtype=torch.uint8, device=DEV)
+    nt = torch.full((B,), n, dtype=torch.int64, device=DEV)
+    idx = torch.empty((B, 512), dtype=torch.int32, device=DEV)
+    pool = torch.full((B, P), -1, dtype=torch.int32, device=DEV)
+    q = [torch.zeros((B, H, 512), dtype=torch.bfloat16, device=DEV)]
+    swa = [torch.zeros((B, 128, 512), dtype=torch.bfloat16, device=DEV)]
+    out = [torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)]
+    swa_len = torch.zeros((B,), dtype=torch.int32, device=DEV)
+    ws = _ws(csa2.OP_LAYER_GROUP, B, n, 512, P, H)
+    csa2.csa2_layer_group(csa2.MODE_FULL, nt, n, codes, scales, kI.to(DEV), qI.to(DEV), w.to(DEV), idx, q, swa,
+                          swa_len, out, ws, pool=pool, form_pool=csa2.POOL_BLOCK_MAX, P=P)
+    torch.cuda.synchronize()
+    gi, gp = idx.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        ref_idx, ref_s = oracle.full_topk(u8(qI)[b], w.numpy()[b], u8(kI)[b], n)
+        check_topk(gi[b], ref_idx, ref_s, np.arange(n), 512)
+        ref_pool, ref_bs = oracle.form_pool_block_max(ref_s, n, P)
+        check_topk(gp[b], ref_pool, ref_bs, np.arange(ref_bs.size), P)
+        assert set((gi[b] // 8).tolist()) <= set(gp[b].tolist())

@@ -174,6 +174,53 @@ def test_pool_recall_tiny():
     assert set((full_idx // 8).tolist()) <= set(pool.tolist())
 
 
+def test_block_max_pool_brute_force_and_small_context():
+    """Block maxima against explicit loops over ragged rows; with at most P
+    blocks the pool is every block."""
+    rng = np.random.default_rng(21)
+    for n in (1, 7, 8, 9, 63, 1000):
+        s = rng.standard_normal(n + 5)
+        pool, bmax = oracle.form_pool_block_max(s, n, P=4096)
+        nb = (n + 7) // 8
+        for j in range(nb):
+            m = -np.inf
+            for t in range(8 * j, min(8 * j + 8, n)):
+                m = max(m, s[t])
+            assert bmax[j] == m
+        assert pool[:nb].tolist() == list(range(nb)) and np.all(pool[nb:] == -1)
+
+
+def test_block_max_pool_recall_guarantee_with_ties():
+    """For P >= k every Full Top-k position lies in a pool block, including
+    integer scores with massive ties and the Top-k tie-break by position."""
+    rng = np.random.default_rng(22)
+    for n, k, P in ((5000, 64, 64), (20000, 512, 512), (20000, 512, 2048), (3000, 100, 150)):
+        for s in (rng.standard_normal(n), rng.integers(0, 5, n).astype(np.float64)):
+            pool, _ = oracle.form_pool_block_max(s, n, P)
+            top = oracle.topk_select(s, np.arange(n), k)
+            assert set((top[top >= 0] // 8).tolist()) <= set(pool[pool >= 0].tolist())
+
+
+def test_mean_key_pool_can_miss_a_top_position():
+    """The mean-key rule gives no such guarantee: a block whose keys point in
+    opposite directions has a near-zero mean key although one of its
+    positions has the largest score."""
+    d = 16
+    q = e4m3_bytes(np.eye(1, d)[0:1] * 4.0)                  # one head on channel 0
+    w = np.array([1.0])
+    k = np.zeros((8 * 4, d))
+    k[0, 0], k[1, 0] = 4.0, -4.0                             # block 0: +4 and -4 -> mean 0
+    for j in range(1, 4):
+        k[8 * j:8 * j + 8, 0] = 1.0                          # blocks 1..3: all +1
+    kb = e4m3_bytes(k)
+    n = 32
+    full_top, s = oracle.full_topk(q, w, kb, n, 1)
+    assert full_top[0] == 0                                  # position 0 has the best score
+    pool_mean, _ = oracle.form_pool(q, w, oracle.block_means(kb, n), P=1)
+    pool_max, _ = oracle.form_pool_block_max(s, n, P=1)
+    assert pool_max[0] == 0 and pool_mean[0] != 0
+
+
 def test_prefill_visible_brute_force():
     for r in (1, 2, 4):
         for p in range(0, 50):
