@@ -229,7 +229,7 @@ class DecodeWorkload:
             if mode == "full" and form_pool:
                 idx, pool = self.idx[g].long(), self.pool.long()
                 hits = total = 0
-                for b in range(self.B):                      # membership per sequence
+                for b in range(idx.shape[0]):                # membership per query row
                     sel = idx[b][idx[b] >= 0]
                     hits += int(torch.isin(sel // 8, pool[b][pool[b] >= 0]).sum())
                     total += int(sel.numel())
@@ -270,6 +270,12 @@ class DecodeWorkload:
         """Positions the Full scans of one step read (for the roofline)."""
         return sum(self.B * min(self.n_end, self.n_cap) for (m, _, _) in self.cfg.groups if m == "full")
 
+    tokens_per_step = property(lambda self: self.B)
+
+    def scan_bytes(self, d_I):
+        """Algorithmic bytes of one Full-scan launch: every key once, one score per query row."""
+        return self.B * min(self.n_end, self.n_cap) * SCAN_BYTES_PER_POS(d_I)
+
     # host-side step for the end-to-end figure: per-step inputs from pinned host memory
     def host_buffers(self):
         torch = self.torch
@@ -297,6 +303,92 @@ class DecodeWorkload:
             d.copy_(s, non_blocking=True)
         for d, s in zip(self.w, hi["w"]):
             d.copy_(s, non_blocking=True)
+        self.step()
+        for d, s in zip(self.h_out, self.out):
+            d.copy_(s, non_blocking=True)
+
+
+class MultiTokenWorkload(DecodeWorkload):
+    """Multi-token decode: R new tokens of each of B sequences per step. The
+    R rows are appended to the caches, then each layer group runs with one
+    query row per token (rows_per_seq = R); every token sees the cache up to
+    itself and attends over its own 128-token window. The windows' bf16 rows
+    (W + R - 1 per sequence and layer) are per-step inputs, like the layer
+    queries."""
+
+    def __init__(self, cfg, device, seed=1234, batch=None, pool_rule="mean"):
+        super().__init__(cfg, device, seed, batch, pool_rule)
+        import synth
+        torch = self.torch
+        B, R = self.B, cfg.tokens
+        self.R, self.rows = R, B * R
+        rows, d_I, H_I, H, W, k, P = self.rows, cfg.d_I, cfg.H_I, cfg.H, cfg.W, cfg.k, cfg.P
+        dev = self.dev
+        n_pre = cfg.n - R                                # the step appends positions n_pre .. n_pre + R - 1
+        G = len(cfg.groups)
+        self.swa = [synth.normal_bf16((B, W + R - 1, 512), seed, "swa", dev, sub=l) for l in range(self.layers)]
+        self.q = [synth.normal_bf16((rows, H, 512), seed, "q", dev, sub=l) for l in range(self.layers)]
+        self.out = [torch.empty((rows, H, 512), dtype=torch.bfloat16, device=dev) for _ in range(self.layers)]
+        self.qI = [synth.normal_e4m3((rows, H_I, d_I), seed, "qI", dev, sub=g) for g in range(G)]
+        self.w = [synth.uniform_f32((rows, H_I), seed, "w", dev, sub=g) for g in range(G)]
+        self.qI_pool = synth.normal_e4m3((rows, H_I, d_I), seed, "qI_pool", dev)
+        self.w_pool = synth.uniform_f32((rows, H_I), seed, "w_pool", dev)
+        self.kv_new = synth.normal_bf16((B, R, 512), seed, "kv_new", dev)
+        self.kI_new = synth.indexer_keys_e4m3((B, R, d_I), seed + 1, dev, bias_prob=cfg.bias_prob)
+        self.idx = [torch.empty((rows, k), dtype=torch.int32, device=dev) for _ in range(G)]
+        self.pool = torch.full((rows, P), -1, dtype=torch.int32, device=dev)
+        self.pos = torch.full((B,), n_pre, dtype=torch.int64, device=dev)
+        n_row = torch.arange(rows, device=dev, dtype=torch.int64) % R + n_pre + 1
+        self.n = n_row.contiguous()
+        self.swa_len = torch.clamp(n_row, max=W).to(torch.int32).contiguous()
+        self.ws = self.csa2.alloc_workspace(
+            self.csa2.workspace_size(self.csa2.OP_LAYER_GROUP, rows, self.n_cap, k, P, H), dev)
+        torch.cuda.synchronize()
+
+    tokens_per_step = property(lambda self: self.rows)
+
+    def scan_bytes(self, d_I):
+        return self.B * self.n_cap * d_I + self.rows * self.n_cap * 4
+
+    def reset_positions(self):
+        self.step_i = 0
+
+    def step(self, events=None):
+        csa2, cfg = self.csa2, self.cfg
+        csa2.csa2_quantize_kv_fp4(self.kv_new, self.codes, self.scales, pos=self.pos)
+        csa2.csa2_append_indexer_k(self.kI_new, self.kI, self.kbar, pos=self.pos)
+        l0 = 0
+        for g, (mode, n_reuse, form_pool) in enumerate(cfg.groups):
+            L = 1 + n_reuse
+            csa2.csa2_layer_group(
+                csa2.MODE_FULL if mode == "full" else csa2.MODE_REINDEX, self.n, self.n_cap, self.codes, self.scales,
+                self.kI, self.qI[g], self.w[g], self.idx[g], self.q[l0:l0 + L], self.swa[l0:l0 + L], self.swa_len,
+                self.out[l0:l0 + L], self.ws, kbar=self.kbar, pool=self.pool,
+                form_pool=self._rule(mode) if form_pool else csa2.POOL_NONE,
+                qI_pool=self.qI_pool if mode == "reindex" else None,
+                w_pool=self.w_pool if mode == "reindex" else None,
+                events=None if events is None else events[g], rows_per_seq=self.R)
+            l0 += L
+        self.step_i += 1
+
+    def host_buffers(self):
+        torch = self.torch
+        self.h_in = {"kv_new": self.kv_new.cpu().pin_memory(), "kI_new": self.kI_new.cpu().pin_memory(),
+                     "swa": [t.cpu().pin_memory() for t in self.swa], "q": [t.cpu().pin_memory() for t in self.q],
+                     "qI": [t.cpu().pin_memory() for t in self.qI], "w": [t.cpu().pin_memory() for t in self.w]}
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.out]
+        hi = self.h_in
+        h2d = hi["kv_new"].numel() * 2 + hi["kI_new"].numel() + sum(t.numel() * 2 for t in hi["swa"]) + \
+            sum(t.numel() * 2 for t in hi["q"]) + sum(t.numel() for t in hi["qI"]) + sum(t.numel() * 4 for t in hi["w"])
+        return h2d, sum(t.numel() * 2 for t in self.h_out)
+
+    def step_e2e(self):
+        hi = self.h_in
+        self.kv_new.copy_(hi["kv_new"], non_blocking=True)
+        self.kI_new.copy_(hi["kI_new"], non_blocking=True)
+        for key, dst in (("swa", self.swa), ("q", self.q), ("qI", self.qI), ("w", self.w)):
+            for d, s in zip(dst, hi[key]):
+                d.copy_(s, non_blocking=True)
         self.step()
         for d, s in zip(self.h_out, self.out):
             d.copy_(s, non_blocking=True)
@@ -466,6 +558,8 @@ def scan_traffic(d_I, positions_per_launch):
 def decode_config(cfg, config_index, batch, world, pool_rule="mean"):
     """The `config` object of a decode bench line (both arms print the same one)."""
     extra = {"pool_rule": "block max of the Full scores"} if pool_rule == "max" else {}
+    if cfg.tokens > 1:
+        extra["tokens_per_sequence"] = cfg.tokens
     return {**extra, "workload": cfg.workload, "config_index": config_index, "batch": batch,
             "context": cfg.n, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}", "topk": cfg.k,
             "swa": cfg.W, "groups": [list(g) for g in cfg.groups], "parallelism": f"replicas{world}",
@@ -483,7 +577,8 @@ def run_csa2(args, world, rank, local):
     cfg = synth.get_config(args.config)
     if cfg.prefill_queries:
         raise SystemExit("the prefill configuration is not a decode bench workload")
-    wl = DecodeWorkload(cfg, dev, seed=1234 + 7919 * rank, batch=args.batch, pool_rule=args.pool_rule)
+    wl_cls = MultiTokenWorkload if cfg.tokens > 1 else DecodeWorkload
+    wl = wl_cls(cfg, dev, seed=1234 + 7919 * rank, batch=args.batch, pool_rule=args.pool_rule)
     G = len(cfg.groups)
     flush = L2Flush(dev)
     total_steps = args.warmup + args.steps
@@ -577,22 +672,23 @@ def run_csa2(args, world, rank, local):
         e1.record()
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-        e2e = {"value": world * wl.B / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e = {"value": world * wl.tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
 
     hbm, hbm_kind = peaks()
     roof = None
     if scan_ms:
         per_launch_pos = wl.B * min(wl.n_end, wl.n_cap)
-        alg = per_launch_pos * SCAN_BYTES_PER_POS(cfg.d_I)
+        alg = wl.scan_bytes(cfg.d_I)
         scan_avg = statistics.mean(scan_ms)
         ach = alg / (scan_avg / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": "k_index_scan (Full indexer scan)", "achieved": round(ach, 1),
                 "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                "traffic": scan_traffic(cfg.d_I, per_launch_pos), "algorithmic_bytes_per_launch": alg,
+                "traffic": scan_traffic(cfg.d_I, per_launch_pos) if cfg.tokens == 1 else None,
+                "algorithmic_bytes_per_launch": alg,
                 "scan_ms": round(scan_avg, 4)}
     res = {
-        "metric": METRIC, "value": world * wl.B / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": world * wl.tokens_per_step / (ms_max / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
         "config": decode_config(cfg, args.config, wl.B, world, args.pool_rule),
@@ -640,7 +736,9 @@ class OracleSample:
         mode = cfg.groups[0][0]
         self.desc = (f"one sequence (batch 1) of the {cfg.workload} step: FP4 append, "
                      f"{'Full scan of all ' + str(n) + ' positions' if mode == 'full' else 'block means + pool + Reindex'}, "
-                     f"Top-{cfg.k}, {self.L} attention layers; gathered rows quantised inside the step")
+                     f"Top-{cfg.k}, {self.L} attention layers; gathered rows quantised inside the step"
+                     + (f"; one of the {cfg.tokens} new tokens of a multi-token step (each costs the same)"
+                        if cfg.tokens > 1 else ""))
 
     def step(self):
         import numpy as np

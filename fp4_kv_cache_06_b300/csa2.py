@@ -52,7 +52,7 @@ class GroupArgs(ctypes.Structure):
         ("q_layers", ctypes.POINTER(_c_p)), ("swa_layers", ctypes.POINTER(_c_p)),
         ("swa_len", _c_p), ("out_layers", ctypes.POINTER(_c_p)),
         ("softmax_scale", _c_f), ("ws", _c_p), ("ws_bytes", _c_sz), ("d_status", _c_p),
-        ("events", ctypes.POINTER(_c_p)), ("n_events", _c_i32),
+        ("events", ctypes.POINTER(_c_p)), ("n_events", _c_i32), ("rows_per_seq", _c_i32),
     ]
 
 
@@ -344,8 +344,12 @@ def csa2_sparse_attn(q, codes, scales, idx, swa, swa_len, out, ws, softmax_scale
 def csa2_layer_group(mode, n, n_max, codes, scales, kI, qI, w, idx, q_layers: Sequence[torch.Tensor],
                      swa_layers: Sequence[torch.Tensor], swa_len, out_layers: Sequence[torch.Tensor], ws,
                      kbar=None, pool=None, form_pool=False, qI_pool=None, w_pool=None, P=2048,
-                     softmax_scale=None, d_status=None, events=None, stream=None):
-    """One layer group: Full or Reindex, then attention for it and each Reuse layer."""
+                     softmax_scale=None, d_status=None, events=None, stream=None, rows_per_seq=1):
+    """One layer group: Full or Reindex, then attention for it and each Reuse layer.
+
+    rows_per_seq R > 1: multi-token decode. The per-row arrays have B rows
+    (R per sequence), the caches B / R sequences, and each SWA array
+    [B / R][W + R - 1][d] holds the linear window rows of each sequence."""
     _need(n, "n", torch.int64, 1)
     _need(codes, "codes", torch.uint8, 3)
     _need(scales, "scales", torch.uint8, 3)
@@ -372,7 +376,11 @@ def csa2_layer_group(mode, n, n_max, codes, scales, kI, qI, w, idx, q_layers: Se
     a.form_pool = int(form_pool)               # False/True -> none/mean-key; or a POOL_* rule
     a.B, a.H, a.d, a.H_I, a.d_I = B, H, d, H_I, d_I
     a.k = idx.shape[1]
-    a.W = swa_layers[0].shape[1]
+    R = max(1, int(rows_per_seq))
+    if B % R:
+        raise ValueError("the row count must be a multiple of rows_per_seq")
+    a.rows_per_seq = R
+    a.W = swa_layers[0].shape[1] - (R - 1)
     a.P = int(P) if pool is None else pool.shape[1]
     a.n_max, a.n_cap = int(n_max), codes.shape[1]
     a.n, a.codes, a.scales, a.kI, a.kbar = n.data_ptr(), codes.data_ptr(), scales.data_ptr(), kI.data_ptr(), (kbar.data_ptr() if kbar is not None else None)

@@ -30,7 +30,7 @@ int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa
 int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
                        int L, int W, int B, int d_I, const int64_t* pos, uint8_t* codes, uint8_t* scales,
                        uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st, cudaStream_t s);
-int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride, int rps,
                       const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
                       int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
                       uint32_t* hist, TopkHdr* hdr, int topk_k, int32_t* st, cudaStream_t s);
@@ -54,8 +54,8 @@ int attn_splits(int B, int H, int k, int W);
 size_t attn_ws_bytes(int B, int H, int k, int W);
 int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                       int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
-                       void* out, void* ws, int32_t* st, cudaStream_t s);
+                       int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
+                       float softmax_scale, void* out, void* ws, int32_t* st, cudaStream_t s);
 
 // ---- bookkeeping --------------------------------------------------------------
 static std::atomic<uint64_t> g_launches{0};
@@ -113,7 +113,7 @@ static int rec(cudaEvent_t e, cudaStream_t s) {
 
 // Full indexer: zero the Top-K header, scan with the fused histogram, select.
 // e_begin / e_end (optional) are recorded around the scan kernel alone.
-static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride, int rps,
                         const int64_t* n, int B, int H_I, int d_I, int64_t n_max, int k, int32_t* idx_out,
                         float* scores_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t e_begin,
                         cudaEvent_t e_end) {
@@ -122,14 +122,14 @@ static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, in
   void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)n_max * 4);
   if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
   if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
-  if ((rc = launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, n_max, nullptr, 0,
+  if ((rc = launch_index_scan(qI, w, kI, kI_seq_stride, rps, n, 1, B, H_I, d_I, n_max, scores, n_max, nullptr, 0,
                               nullptr, topk_ws_hist(tk), topk_ws_hdr(tk, B), k, st, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
   return launch_topk(scores, nullptr, n_max, n, 1, B, n_max, k, idx_out, tk, true, s);
 }
 
-static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, int64_t kbar_seq_stride,
+static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, int64_t kbar_seq_stride, int rps,
                         const int64_t* n, int B, int H_I, int d_I, int64_t n_max, int P, int32_t* pool_out,
                         void* ws, int32_t* st, cudaStream_t s) {
   int rc;
@@ -137,13 +137,13 @@ static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, 
   float* scores = static_cast<float*>(ws);
   void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)nb_max * 4);
   if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
-  if ((rc = launch_index_scan(qI, w, kbar, kbar_seq_stride, n, kBlock, B, H_I, d_I, nb_max, scores, nb_max,
+  if ((rc = launch_index_scan(qI, w, kbar, kbar_seq_stride, rps, n, kBlock, B, H_I, d_I, nb_max, scores, nb_max,
                               nullptr, 0, nullptr, topk_ws_hist(tk), topk_ws_hdr(tk, B), P, st, s)) != CSA2_OK)
     return rc;
   return launch_topk(scores, nullptr, nb_max, n, kBlock, B, nb_max, P, pool_out, tk, true, s);
 }
 
-static int reindex_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+static int reindex_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride, int rps,
                            const int64_t* n, const int32_t* pool, int P, int B, int H_I, int d_I, int k,
                            int32_t* idx_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t e_begin,
                            cudaEvent_t e_end) {
@@ -156,7 +156,7 @@ static int reindex_indexer(const uint8_t* qI, const float* w, const uint8_t* kI,
   if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
   // The pool scan writes every one of the P*8 slots of every row (absent
   // positions carry cand_pos -1), so Top-K takes all slots of each row.
-  if (P > 0 && (rc = launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, INT64_MAX, scores, slots,
+  if (P > 0 && (rc = launch_index_scan(qI, w, kI, kI_seq_stride, rps, n, 1, B, H_I, d_I, INT64_MAX, scores, slots,
                                        pool, P, cpos, topk_ws_hist(tk), topk_ws_hdr(tk, B), k, st, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
@@ -284,7 +284,7 @@ int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int6
   if (!qI || !w || !kI || !n || !scores || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
   const int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
-  return launch_index_scan(qI, w, kI, kI_seq_stride, n, 1, B, H_I, d_I, n_max, scores, scores_stride,
+  return launch_index_scan(qI, w, kI, kI_seq_stride, 1, n, 1, B, H_I, d_I, n_max, scores, scores_stride,
                            nullptr, 0, nullptr, nullptr, nullptr, 0, d_status, static_cast<cudaStream_t>(stream));
 }
 
@@ -313,7 +313,7 @@ int csa2_index_full(const uint8_t* qI, const float* w, const uint8_t* kI, int64_
   if (!ws_ok(ws, ws_bytes, ws_index_full(B, n_max))) return CSA2_ERR_WORKSPACE;
   int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
-  return full_indexer(qI, w, kI, kI_seq_stride, n, B, H_I, d_I, n_max, k, idx_out, scores_out, ws, d_status,
+  return full_indexer(qI, w, kI, kI_seq_stride, 1, n, B, H_I, d_I, n_max, k, idx_out, scores_out, ws, d_status,
                       static_cast<cudaStream_t>(stream), nullptr, nullptr);
 }
 
@@ -327,7 +327,7 @@ int csa2_form_pool(const uint8_t* qI, const float* w, const uint8_t* kbar, int64
   if (!ws_ok(ws, ws_bytes, ws_form_pool(B, n_max))) return CSA2_ERR_WORKSPACE;
   int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
-  return pool_indexer(qI, w, kbar, kbar_seq_stride, n, B, H_I, d_I, n_max, P, pool_out, ws, d_status,
+  return pool_indexer(qI, w, kbar, kbar_seq_stride, 1, n, B, H_I, d_I, n_max, P, pool_out, ws, d_status,
                       static_cast<cudaStream_t>(stream));
 }
 
@@ -354,7 +354,7 @@ int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t* kI, int
   if (!ws_ok(ws, ws_bytes, ws_reindex(B, P))) return CSA2_ERR_WORKSPACE;
   int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
-  return reindex_indexer(qI, w, kI, kI_seq_stride, n, pool, P, B, H_I, d_I, k, idx_out, ws, d_status,
+  return reindex_indexer(qI, w, kI, kI_seq_stride, 1, n, pool, P, B, H_I, d_I, k, idx_out, ws, d_status,
                          static_cast<cudaStream_t>(stream), nullptr, nullptr);
 }
 
@@ -376,7 +376,8 @@ int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d, const uint8
   int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
   return launch_sparse_attn(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
-                            swa_tail != 0, swa_len, softmax_scale, out, ws, d_status, static_cast<cudaStream_t>(stream));
+                            swa_tail != 0, 1, swa_len, softmax_scale, out, ws, d_status,
+                            static_cast<cudaStream_t>(stream));
 }
 
 static cudaEvent_t group_event(const csa2_group_args* a, int i) {
@@ -392,6 +393,8 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   if (a->B == 0) return CSA2_OK;
   if (!a->n || !a->codes || !a->scales || !a->kI || !a->qI || !a->w || !a->swa_len) return CSA2_ERR_INVALID_ARG;
   if (a->form_pool < CSA2_POOL_NONE || a->form_pool > CSA2_POOL_BLOCK_MAX) return CSA2_ERR_INVALID_ARG;
+  if (a->rows_per_seq < 0 || a->rows_per_seq > 64 || (a->rows_per_seq > 1 && a->B % a->rows_per_seq != 0))
+    return CSA2_ERR_INVALID_ARG;
   if (a->form_pool == CSA2_POOL_BLOCK_MAX && a->mode != CSA2_MODE_FULL) return CSA2_ERR_INVALID_ARG;
   if ((a->form_pool || a->mode == CSA2_MODE_REINDEX) && !a->pool) return CSA2_ERR_INVALID_ARG;
   if (a->form_pool == CSA2_POOL_MEAN_KEY && !a->kbar) return CSA2_ERR_INVALID_ARG;
@@ -406,15 +409,16 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   if (rc != CSA2_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t nbc = (a->n_cap + kBlock - 1) / kBlock;
+  const int rps = a->rows_per_seq > 1 ? a->rows_per_seq : 1;
   const uint8_t* qp = a->qI_pool ? a->qI_pool : a->qI;
   const float* wp = a->w_pool ? a->w_pool : a->w;
   // events: [0] indexer scan begins, [1] scan ends, [2] Top-K (and pool) done,
   // [3 + l] attention of layer l done
   if (a->mode == CSA2_MODE_FULL) {
-    rc = full_indexer(a->qI, a->w, a->kI, a->n_cap, a->n, a->B, a->H_I, a->d_I, a->n_max, a->k, a->idx, nullptr,
+    rc = full_indexer(a->qI, a->w, a->kI, a->n_cap, rps, a->n, a->B, a->H_I, a->d_I, a->n_max, a->k, a->idx, nullptr,
                       a->ws, a->d_status, s, group_event(a, 0), group_event(a, 1));
     if (rc == CSA2_OK && a->form_pool == CSA2_POOL_MEAN_KEY)
-      rc = pool_indexer(qp, wp, a->kbar, nbc, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
+      rc = pool_indexer(qp, wp, a->kbar, nbc, rps, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
                         a->d_status, s);
     if (rc == CSA2_OK && a->form_pool == CSA2_POOL_BLOCK_MAX)   // the Full scores are still at ws
       rc = launch_pool_block_max(static_cast<const float*>(a->ws), a->n_max, a->n, a->B, a->n_max, a->P, a->pool,
@@ -422,19 +426,21 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   } else {
     if ((rc = rec(group_event(a, 0), s)) != CSA2_OK) return rc;
     if (a->form_pool)
-      rc = pool_indexer(qp, wp, a->kbar, nbc, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
+      rc = pool_indexer(qp, wp, a->kbar, nbc, rps, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
                         a->d_status, s);
     if (rc == CSA2_OK)
-      rc = reindex_indexer(a->qI, a->w, a->kI, a->n_cap, a->n, a->pool, a->P, a->B, a->H_I, a->d_I, a->k,
+      rc = reindex_indexer(a->qI, a->w, a->kI, a->n_cap, rps, a->n, a->pool, a->P, a->B, a->H_I, a->d_I, a->k,
                            a->idx, a->ws, a->d_status, s, nullptr, group_event(a, 1));
   }
   if (rc != CSA2_OK) return rc;
   if ((rc = rec(group_event(a, 2), s)) != CSA2_OK) return rc;
   for (int l = 0; l <= a->n_reuse; ++l) {
     if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
+    // one row per sequence: the layer's SWA ring (W rows, present keys first);
+    // rps rows per sequence: W + rps - 1 linear rows, each window ending at its token
     rc = launch_sparse_attn(a->q_layers[l], a->B, a->H, a->codes, a->scales, a->n_cap, a->n_cap, a->idx, a->k,
-                            a->swa_layers[l], a->W, a->W, 0, a->swa_len, a->softmax_scale, a->out_layers[l], a->ws,
-                            a->d_status, s);
+                            a->swa_layers[l], rps > 1 ? a->W + rps - 1 : a->W, a->W, rps > 1 ? 1 : 0, rps,
+                            a->swa_len, a->softmax_scale, a->out_layers[l], a->ws, a->d_status, s);
     if (rc != CSA2_OK) return rc;
     if ((rc = rec(group_event(a, 3 + l), s)) != CSA2_OK) return rc;
   }
@@ -486,7 +492,7 @@ int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
   for (int l = 0; l <= a->n_reuse; ++l) {
     if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
     rc = launch_sparse_attn(a->q_layers[l], a->Q, a->H, a->codes, a->scales, 0, a->n_keys, a->idx, a->k,
-                            a->swa_layers[l], 1, a->W, 1, a->swa_len, a->softmax_scale, a->out_layers[l], aws,
+                            a->swa_layers[l], 1, a->W, 1, 1, a->swa_len, a->softmax_scale, a->out_layers[l], aws,
                             a->d_status, s);
     if (rc != CSA2_OK) return rc;
     if ((rc = rec(ev(3 + l), s)) != CSA2_OK) return rc;

@@ -38,7 +38,7 @@ constexpr int kScanRowsPerWarpIter = 16 * kScanTilesPerIter;
 template <int DI, bool SRC_POOL>
 __global__ void __launch_bounds__(kScanThreads) k_index_scan(
     const uint8_t* __restrict__ qI, const float* __restrict__ w, const uint8_t* __restrict__ kI,
-    int64_t kI_seq_stride, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max,
+    int64_t kI_seq_stride, int rps, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max,
     int64_t rows_per_cta, float* __restrict__ scores, int64_t scores_stride,
     const int32_t* __restrict__ pool, int P, int32_t* __restrict__ cand_pos,
     uint32_t* __restrict__ hist, TopkHdr* __restrict__ hdr, int topk_k, int32_t* st) {
@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(kScanThreads) k_index_scan(
   }
   const float w0 = (2 * t < H_I) ? w[(int64_t)b * H_I + 2 * t] : 0.f;
   const float w1 = (2 * t + 1 < H_I) ? w[(int64_t)b * H_I + 2 * t + 1] : 0.f;
-  const uint8_t* kseq = kI + (int64_t)b * kI_seq_stride * DI;
+  const uint8_t* kseq = kI + (int64_t)(b / rps) * kI_seq_stride * DI;   // rps query rows per sequence
   float* srow = scores + (int64_t)b * scores_stride;
 
   for (int64_t base = c0 + (int64_t)warp * kScanRowsPerWarpIter; base < c1;
@@ -155,7 +155,7 @@ constexpr int kTmaSmem = kTmaStages * kTmaTile + 1024 + 64;
 
 __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
     const __grid_constant__ CUtensorMap map_k, const uint8_t* __restrict__ qI, const float* __restrict__ w,
-    int64_t kI_seq_stride, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max, int tiles_per_cta,
+    int64_t kI_seq_stride, int rps, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max, int tiles_per_cta,
     float* __restrict__ scores, int64_t scores_stride, uint32_t* __restrict__ hist, TopkHdr* __restrict__ hdr,
     int topk_k, int32_t* st) {
   __shared__ uint32_t sh_hist[kHistBins];
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
         if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kTmaStages) & 1) ^ 1)) { report(st, CSA2_ERR_TIMEOUT); break; }
         tc::mbar_expect_tx(bar_full + 8 * s, kTmaTile);
         tc::tma_load_2d(base + s * kTmaTile, &map_k, 0,
-                        (int32_t)((int64_t)b * kI_seq_stride + (t0 + i) * kTmaRows), bar_full + 8 * s);
+                        (int32_t)((int64_t)(b / rps) * kI_seq_stride + (t0 + i) * kTmaRows), bar_full + 8 * s);
       }
     }
   } else {                                         // consumers: warp w owns m-tile w of every tile
@@ -278,7 +278,7 @@ static int64_t scan_rows_per_cta(int B, int64_t rows) {
   return per;
 }
 
-int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,
+int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride, int rps,
                       const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
                       int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
                       uint32_t* hist, TopkHdr* hdr, int topk_k, int32_t* st, cudaStream_t s) {
@@ -287,7 +287,7 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
   if (rows == 0 || B == 0) return CSA2_OK;
   if (!use_pool && d_I == 128 && tma_scan_init) {
     // the key rows of all sequences as one 2-D tensor [rows][128 B]
-    const uint64_t total_rows = (uint64_t)(B - 1) * (uint64_t)kI_seq_stride + (uint64_t)n_max;
+    const uint64_t total_rows = (uint64_t)((B - 1) / rps) * (uint64_t)kI_seq_stride + (uint64_t)n_max;
     CUtensorMap map;
     if (make_tmap_rows128(&map, kI, total_rows, 128, kTmaRows)) {
       const int64_t tiles = (n_max + kTmaRows - 1) / kTmaRows;
@@ -299,7 +299,7 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
       const int tpc = (int)((tiles + per_seq - 1) / per_seq);
       per_seq = (tiles + tpc - 1) / tpc;
       dim3 grid((unsigned)per_seq, (unsigned)B);
-      k_index_scan_tma<<<grid, kTmaThreads, kTmaSmem, s>>>(map, qI, w, kI_seq_stride, n, len_div, H_I, n_max, tpc,
+      k_index_scan_tma<<<grid, kTmaThreads, kTmaSmem, s>>>(map, qI, w, kI_seq_stride, rps, n, len_div, H_I, n_max, tpc,
                                                            scores, scores_stride, hist, hdr, topk_k, st);
       count_launch();
       return launch_status();
@@ -308,7 +308,7 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
   const int64_t per = scan_rows_per_cta(B, rows);
   dim3 grid((unsigned)((rows + per - 1) / per), (unsigned)B);
 #define CSA2_SCAN(DI_, POOL_)                                                                   \
-  k_index_scan<DI_, POOL_><<<grid, kScanThreads, 0, s>>>(qI, w, kI, kI_seq_stride, n, len_div, H_I, n_max, \
+  k_index_scan<DI_, POOL_><<<grid, kScanThreads, 0, s>>>(qI, w, kI, kI_seq_stride, rps, n, len_div, H_I, n_max, \
                                                          per, scores, scores_stride, pool, P,     \
                                                          cand_pos, hist, hdr, topk_k, st)
   if (d_I == 128) {

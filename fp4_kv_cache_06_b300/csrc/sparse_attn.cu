@@ -75,9 +75,9 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
 // ---- host ------------------------------------------------------------------
 int launch_sparse_attn_tc(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                          int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
-                          void* out, float* part_o, float* part_ml, int splits, int tps, int32_t* st,
-                          cudaStream_t s);
+                          int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
+                          float softmax_scale, void* out, float* part_o, float* part_ml, int splits, int tps,
+                          int32_t* st, cudaStream_t s);
 
 // Split-K count. The attention kernel runs one CTA per SM (its shared memory
 // and all 512 TMEM columns). A batch that fills the machine runs unsplit (a
@@ -111,8 +111,8 @@ size_t attn_ws_bytes(int B, int H, int k, int W) {
 
 int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                       int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
-                       void* out, void* ws, int32_t* st, cudaStream_t s) {
+                       int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
+                       float softmax_scale, void* out, void* ws, int32_t* st, cudaStream_t s) {
   if (B == 0) return CSA2_OK;
   if (H < 1 || H > 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
   const int splits = attn_splits(B, H, k, W);
@@ -126,7 +126,8 @@ int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const 
     part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + ((po + 255) & ~(size_t)255));
   }
   int rc = launch_sparse_attn_tc(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
-                                 swa_tail, swa_len, softmax_scale, out, part_o, part_ml, splits, tps, st, s);
+                                 swa_tail, rps < 1 ? 1 : rps, swa_len, softmax_scale, out, part_o, part_ml, splits,
+                                 tps, st, s);
   if (rc != CSA2_OK || splits == 1) return rc;
   const dim3 grid((unsigned)(((kD / 4) * H + 127) / 128), (unsigned)B);
   auto kern = splits <= 4 ? k_attn_merge<4> : splits <= 8 ? k_attn_merge<8> : k_attn_merge<16>;

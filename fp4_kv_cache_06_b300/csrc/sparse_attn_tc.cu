@@ -137,7 +137,7 @@ __device__ __forceinline__ uint32_t ldg_hint_u8(const void* p, uint64_t pol) {
 __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     const __nv_bfloat16* __restrict__ q, int H, const uint8_t* __restrict__ codes,
     const uint8_t* __restrict__ scales, int64_t kv_seq_stride, int64_t n_cap, const int32_t* __restrict__ idx,
-    int k, const __nv_bfloat16* __restrict__ swa, int64_t swa_seq_stride, int W, int swa_tail,
+    int k, const __nv_bfloat16* __restrict__ swa, int64_t swa_seq_stride, int W, int swa_tail, int rps,
     const int32_t* __restrict__ swa_len, float scale_log2, int splits, int tiles_per_split,
     __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
   extern __shared__ unsigned char smem_raw[];
@@ -193,6 +193,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   cp_async_commit();
   // the SWA length is clamped without a branch, so nothing waits on its load
   const int slen_in = swa_len[b];
+  // row b reads the caches of sequence b / rps; with rps > 1 the sequence's
+  // SWA rows are linear and row b's window starts b % rps rows in
+  const int64_t kv_row0 = (int64_t)(b / rps) * kv_seq_stride;
+  const int64_t swa_row0 = (int64_t)(b / rps) * swa_seq_stride + (b % rps);
   const int slen = min(max(slen_in, 0), W);
 
   // Row sources of tile j (called by a whole warp pair: row p of the tile).
@@ -202,10 +206,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     const int r = (t_begin + j) * kTT + p;
     int64_t src = -1;
     if (r < W) {
-      if (r < slen) src = -2 - ((int64_t)b * swa_seq_stride + (swa_tail ? W - slen : 0) + r);
+      if (r < slen) src = -2 - (swa_row0 + (swa_tail ? W - slen : 0) + r);
     } else if (r - W < k) {
       const int32_t pos = idx[(int64_t)b * k + (r - W)];
-      if (pos >= 0 && pos < n_cap) src = (int64_t)b * kv_seq_stride + pos;
+      if (pos >= 0 && pos < n_cap) src = kv_row0 + pos;
       else if (pos >= n_cap) report(st, CSA2_ERR_DEVICE_BOUNDS);
     }
     sSrc[slot * kTT + p] = src;
@@ -552,14 +556,14 @@ int attn_tc_init_attributes() {
 
 int launch_sparse_attn_tc(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                          int64_t swa_seq_stride, int W, int swa_tail, const int32_t* swa_len, float softmax_scale,
-                          void* out, float* part_o, float* part_ml, int splits, int tps, int32_t* st,
-                          cudaStream_t s) {
+                          int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
+                          float softmax_scale, void* out, float* part_o, float* part_ml, int splits, int tps,
+                          int32_t* st, cudaStream_t s) {
   dim3 grid((unsigned)splits, (unsigned)B);
   const cudaError_t e = launch_pdl(
       k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, reinterpret_cast<const __nv_bfloat16*>(q), H,
       codes, scales, kv_seq_stride, n_cap, idx, k, reinterpret_cast<const __nv_bfloat16*>(swa), swa_seq_stride, W,
-      swa_tail, swa_len, softmax_scale * 1.4426950408889634f, splits, tps, reinterpret_cast<__nv_bfloat16*>(out),
+      swa_tail, rps, swa_len, softmax_scale * 1.4426950408889634f, splits, tps, reinterpret_cast<__nv_bfloat16*>(out),
       part_o, part_ml, st);
   count_launch();
   return launch_status(e);

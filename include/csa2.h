@@ -325,6 +325,18 @@ typedef struct csa2_group_args {
                             scan ends, [2] Top-K (and pool) done, [3 + l]
                             layer l's attention done                         */
   int32_t n_events;      /* length of `events` (0 = none)                     */
+  int32_t rows_per_seq;  /* query rows per sequence, R (0 or 1: one). With
+                            R > 1 (multi-token decode: R new tokens of each
+                            sequence decoded in one step) B counts rows, and
+                            row r reads the caches of sequence r / R (codes,
+                            scales, kI, kbar have B / R sequences); n, qI, w,
+                            pool, idx, swa_len, q and out stay per row; each
+                            layer's SWA array holds W + R - 1 linear rows per
+                            sequence (tokens p - W + 1 .. p + R - 1 for its
+                            first new token p), row r's window is rows
+                            r % R .. r % R + W - 1 of it, with its swa_len[r]
+                            present keys at the window's end. B % R == 0,
+                            R <= 64.                                          */
 } csa2_group_args;
 
 /* Run one CSA2 layer group: the first layer (Full: scan all positions,

@@ -28,6 +28,7 @@ class Config:
     n_start: int = 0       # positions cached before the first step (stack config)
     prefill_queries: int = 0
     ratio: int = 1         # compression ratio (tokens per main-KV entry)
+    tokens: int = 1        # new tokens per sequence and step (multi-token decode)
     extra: dict = field(default_factory=dict)
 
 
@@ -43,6 +44,8 @@ CONFIGS = {
     5: Config("cfg5", "decoder_stack20_b4_ctx1048576_256steps", B=4, n=1048576,
               n_start=1048320, steps=256,
               groups=(("full", 3, True),) + (("reindex", 3, False),) * 4),
+    6: Config("cfg6", "decoder_group_full3reuse_b32x4tok_ctx131072", B=32, n=131072, bias_prob=0.05,
+              groups=(("full", 3, False),), tokens=4),
 }
 
 
