@@ -394,9 +394,115 @@ class MultiTokenWorkload(DecodeWorkload):
             d.copy_(s, non_blocking=True)
 
 
+class EncoderDecodeWorkload(DecodeWorkload):
+    """Decode through the encoder's layer groups at compression ratio r. Every
+    group keeps its own caches (its Full layer's main KV and indexer K). Each
+    step appends the token's SWA row to every layer and, when the token
+    completes an entry (every r-th token), one compressed entry to every
+    group's caches; the append kernel decides that on the device and writes
+    the token's visible entry count and SWA length, which the groups then use.
+    The entries themselves are inputs (merging r tokens needs weights)."""
+
+    def __init__(self, cfg, device, seed=1234, batch=None, pool_rule="mean"):
+        import torch
+        import synth
+        from fp4_kv_cache_06_b300 import csa2
+        self.torch, self.csa2, self.cfg, self.pool_rule, self.dev = torch, csa2, cfg, pool_rule, device
+        B = self.B = batch or cfg.B
+        r, d_I, H_I, H, W, k, P = cfg.ratio, cfg.d_I, cfg.H_I, cfg.H, cfg.W, cfg.k, cfg.P
+        self.n_cap = self.n_end = cfg.n                  # entries per group cache after the last step
+        self.t_first = cfg.n * r - cfg.steps             # token of the first step; the last sees all n entries
+        e_pre = self.t_first // r                        # entries complete before the first step
+        G = len(cfg.groups)
+        self.layers = sum(1 + g[1] for g in cfg.groups)
+        dev, u8 = device, torch.uint8
+        self.codes, self.scales, self.kI, self.kbar = [], [], [], []
+        chunk = 1 << 17
+        for g in range(G):
+            codes = torch.empty((B, self.n_cap, 256), dtype=u8, device=dev)
+            scales = torch.empty((B, self.n_cap, 32), dtype=u8, device=dev)
+            kI = torch.empty((B, self.n_cap, d_I), dtype=u8, device=dev)
+            kbar = torch.zeros((B, (self.n_cap + 7) // 8, d_I), dtype=u8, device=dev)
+            for b in range(B):
+                for c0 in range(0, e_pre, chunk):
+                    rr = min(chunk, e_pre - c0)
+                    x = synth.normal_bf16((1, rr, 512), seed, "kv", dev, sub=(g * 64 + b) * 4096 + c0 // chunk)
+                    csa2.csa2_quantize_kv_fp4(x, codes[b:b + 1], scales[b:b + 1],
+                                              pos=torch.tensor([c0], dtype=torch.int64, device=dev))
+                kI[b, :e_pre] = synth.indexer_keys_e4m3((e_pre, d_I), seed, dev, sub=g * 64 + b)
+            csa2.csa2_block_means(kI, torch.full((B,), e_pre, dtype=torch.int64, device=dev), kbar, n_max=e_pre)
+            self.codes.append(codes); self.scales.append(scales); self.kI.append(kI); self.kbar.append(kbar)
+        self.swa = [synth.normal_bf16((B, W, 512), seed, "swa", dev, sub=l) for l in range(self.layers)]
+        self.q = [synth.normal_bf16((B, H, 512), seed, "q", dev, sub=l) for l in range(self.layers)]
+        self.out = [torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev) for _ in range(self.layers)]
+        self.qI = [synth.normal_e4m3((B, H_I, d_I), seed, "qI", dev, sub=g) for g in range(G)]
+        self.w = [synth.uniform_f32((B, H_I), seed, "w", dev, sub=g) for g in range(G)]
+        self.kv_new = [synth.normal_bf16((B, 512), seed, "kv_new", dev, sub=g) for g in range(G)]
+        self.kI_new = [synth.indexer_keys_e4m3((B, d_I), seed + 1, dev, sub=g) for g in range(G)]
+        self.swa_new = [synth.normal_bf16((B, 512), seed, "swa_new", dev, sub=l) for l in range(self.layers)]
+        self.idx = [torch.empty((B, k), dtype=torch.int32, device=dev) for _ in range(G)]
+        self.pos = torch.full((B,), self.t_first, dtype=torch.int64, device=dev)
+        self.n = torch.zeros((B,), dtype=torch.int64, device=dev)            # written by the append
+        self.swa_len = torch.zeros((B,), dtype=torch.int32, device=dev)      # written by the append
+        self.ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_LAYER_GROUP, B, self.n_cap, k, P, H), dev)
+        self.step_i = 0
+        torch.cuda.synchronize()
+
+    def reset_positions(self):
+        self.step_i = 0
+        self.pos.fill_(self.t_first)
+
+    def pool_recall(self):
+        return None
+
+    def step(self, events=None):
+        csa2, cfg = self.csa2, self.cfg
+        if self.step_i > 0:
+            self.pos.add_(1)
+        l0 = 0
+        for g, (mode, n_reuse, _) in enumerate(cfg.groups):
+            L = 1 + n_reuse
+            csa2.csa2_append_step_ratio(self.kv_new[g], self.kI_new[g], self.swa_new[l0:l0 + L], self.swa[l0:l0 + L],
+                                        self.pos, cfg.ratio, self.codes[g], self.scales[g], self.kI[g], self.kbar[g],
+                                        n_vis_out=self.n if g == 0 else None,
+                                        swa_len_out=self.swa_len if g == 0 else None)
+            l0 += L
+        l0 = 0
+        for g, (mode, n_reuse, _) in enumerate(cfg.groups):
+            L = 1 + n_reuse
+            csa2.csa2_layer_group(csa2.MODE_FULL, self.n, self.n_cap, self.codes[g], self.scales[g], self.kI[g],
+                                  self.qI[g], self.w[g], self.idx[g], self.q[l0:l0 + L], self.swa[l0:l0 + L],
+                                  self.swa_len, self.out[l0:l0 + L], self.ws,
+                                  events=None if events is None else events[g])
+            l0 += L
+        self.step_i += 1
+
+    def host_buffers(self):
+        torch = self.torch
+        self.h_in = {"kv_new": [t.cpu().pin_memory() for t in self.kv_new],
+                     "kI_new": [t.cpu().pin_memory() for t in self.kI_new],
+                     "swa_new": [t.cpu().pin_memory() for t in self.swa_new],
+                     "q": [t.cpu().pin_memory() for t in self.q], "qI": [t.cpu().pin_memory() for t in self.qI],
+                     "w": [t.cpu().pin_memory() for t in self.w]}
+        self.h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in self.out]
+        size = {"kv_new": 2, "kI_new": 1, "swa_new": 2, "q": 2, "qI": 1, "w": 4}
+        h2d = sum(t.numel() * size[key] for key, ts in self.h_in.items() for t in ts)
+        return h2d, sum(t.numel() * 2 for t in self.h_out)
+
+    def step_e2e(self):
+        for key in ("kv_new", "kI_new", "swa_new", "q", "qI", "w"):
+            for d, s in zip(getattr(self, key), self.h_in[key]):
+                d.copy_(s, non_blocking=True)
+        self.step()
+        for d, s in zip(self.h_out, self.out):
+            d.copy_(s, non_blocking=True)
+
+
 class PrefillWorkload:
-    """One encoder prefill chunk: queries at tokens p0..p0+Q-1 over a shared FP4
-    cache of n compressed entries (ratio 2), Full + Reuse layers."""
+    """One encoder prefill chunk: queries at tokens p0..p0+Q-1 over a cache of n
+    compressed entries (ratio 2), one Full + Reuse group per entry of
+    cfg.groups. With cfg.group_caches every group has its own caches (its Full
+    layer's main KV and indexer K); otherwise they share one."""
 
     def __init__(self, cfg, device, seed=1234, queries=None):
         import torch
@@ -409,18 +515,25 @@ class PrefillWorkload:
         tokens = n * cfg.ratio                               # context incl. the chunk
         self.p0 = tokens - Q
         dev = device
-        self.codes = torch.empty((n, 256), dtype=torch.uint8, device=dev)
-        self.scales = torch.empty((n, 32), dtype=torch.uint8, device=dev)
+        G = self.G = len(cfg.groups)
+        n_caches = G if cfg.group_caches else 1
+        self.codes, self.scales, self.kI = [], [], []
         chunk = 1 << 16
-        for c0 in range(0, n, chunk):
-            r = min(chunk, n - c0)
-            x = synth.normal_bf16((1, r, 512), seed, "kv", dev, sub=c0 // chunk)
-            csa2.csa2_quantize_kv_fp4(x, self.codes[None], self.scales[None],
-                                      pos=torch.tensor([c0], dtype=torch.int64, device=dev))
-        self.kI = synth.indexer_keys_e4m3((n, cfg.d_I), seed, dev)
-        self.qI = synth.normal_e4m3((Q, cfg.H_I, cfg.d_I), seed, "qI", dev)
-        self.w = synth.uniform_f32((Q, cfg.H_I), seed, "w", dev)
-        self.layers = 1 + cfg.groups[0][1]
+        for c in range(n_caches):
+            codes = torch.empty((n, 256), dtype=torch.uint8, device=dev)
+            scales = torch.empty((n, 32), dtype=torch.uint8, device=dev)
+            for c0 in range(0, n, chunk):
+                r = min(chunk, n - c0)
+                x = synth.normal_bf16((1, r, 512), seed, "kv", dev, sub=c * 4096 + c0 // chunk)
+                csa2.csa2_quantize_kv_fp4(x, codes[None], scales[None],
+                                          pos=torch.tensor([c0], dtype=torch.int64, device=dev))
+            self.codes.append(codes)
+            self.scales.append(scales)
+            self.kI.append(synth.indexer_keys_e4m3((n, cfg.d_I), seed, dev, sub=c))
+        self.qI = [synth.normal_e4m3((Q, cfg.H_I, cfg.d_I), seed, "qI", dev, sub=g) for g in range(G)]
+        self.w = [synth.uniform_f32((Q, cfg.H_I), seed, "w", dev, sub=g) for g in range(G)]
+        self.group_layers = [1 + g[1] for g in cfg.groups]
+        self.layers = sum(self.group_layers)
         self.q = [synth.normal_bf16((Q, H, 512), seed, "q", dev, sub=l) for l in range(self.layers)]
         self.swa = [synth.normal_bf16((Q + W - 1, 512), seed, "swa", dev, sub=l) for l in range(self.layers)]
         self.out = [torch.empty((Q, H, 512), dtype=torch.bfloat16, device=dev) for _ in range(self.layers)]
@@ -433,8 +546,13 @@ class PrefillWorkload:
         torch.cuda.synchronize()
 
     def step(self, events=None):
-        self.csa2.csa2_prefill_group(self.n_vis, self.codes, self.scales, self.kI, self.qI, self.w, self.idx,
-                                     self.q, self.swa, self.swa_len, self.out, self.ws, events=events)
+        l0 = 0
+        for g in range(self.G):
+            c, L = (g if self.cfg.group_caches else 0), self.group_layers[g]
+            self.csa2.csa2_prefill_group(self.n_vis, self.codes[c], self.scales[c], self.kI[c], self.qI[g], self.w[g],
+                                         self.idx, self.q[l0:l0 + L], self.swa[l0:l0 + L], self.swa_len,
+                                         self.out[l0:l0 + L], self.ws, events=None if events is None else events[g])
+            l0 += L
 
     def gemm_flops(self):
         return 2.0 * self.Q * self.cfg.H_I * self.n_keys * self.cfg.d_I
@@ -460,8 +578,7 @@ def run_prefill(args, world, rank, local):
         e = torch.cuda.Event(enable_timing=True, external=True)
         e.record()
         return e
-    nev = 3 + wl.layers
-    evs = [[mk() for _ in range(nev)] for _ in range(args.steps)]
+    evs = [[[mk() for _ in range(3 + L)] for L in wl.group_layers] for _ in range(args.steps)]
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
     torch.cuda.synchronize()
     launches0 = csa2.launch_count()
@@ -484,9 +601,10 @@ def run_prefill(args, world, rank, local):
     barrier(world)
     ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
     ms_max = max_over_ranks(ms, world, dev)
-    gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    attn_ms = statistics.mean(e[2 + j].elapsed_time(e[3 + j]) for e in evs for j in range(wl.layers))
+    gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for es in evs for e in es)
+    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for es in evs for e in es)
+    attn_ms = statistics.mean(e[2 + j].elapsed_time(e[3 + j]) for es in evs for g, e in enumerate(es)
+                              for j in range(wl.group_layers[g]))
     bf16 = 1765.8
     try:
         with open(PEAKS_FILE) as f:
@@ -497,13 +615,17 @@ def run_prefill(args, world, rank, local):
     fp8_peak = 2 * bf16
     ach = wl.gemm_flops() / (gemm_ms / 1e3) / 1e12
     res = {
-        "metric": "CSA2 prefill query tokens/s per encoder group (ratio 2); % of B300 FP8 tensor roofline",
+        "metric": ("CSA2 prefill query tokens/s per encoder group (ratio 2); % of B300 FP8 tensor roofline"
+                   if wl.G == 1 else
+                   f"CSA2 prefill query tokens/s through the {wl.G}-group encoder stack (ratio 2); "
+                   "% of B300 FP8 tensor roofline"),
         "value": world * wl.Q / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
         "config": {"workload": cfg.workload, "config_index": args.config, "queries": wl.Q, "entries": wl.n_keys,
                    "first_query_token": wl.p0, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}",
-                   "topk": cfg.k, "swa": cfg.W, "layers": wl.layers, "parallelism": f"replicas{world}",
+                   "topk": cfg.k, "swa": cfg.W, "layers": wl.layers, "groups": [list(g) for g in cfg.groups],
+                   "separate_group_caches": cfg.group_caches, "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (2 GiB score matrix per step)"},
         "roofline": {"bound": "tensor", "kernel": "k_prefill_index (tcgen05 FP8 indexer GEMM)",
                      "achieved": round(ach, 1), "peak": fp8_peak, "peak_kind": kind, "unit": "TFLOP/s",
@@ -577,7 +699,8 @@ def run_csa2(args, world, rank, local):
     cfg = synth.get_config(args.config)
     if cfg.prefill_queries:
         raise SystemExit("the prefill configuration is not a decode bench workload")
-    wl_cls = MultiTokenWorkload if cfg.tokens > 1 else DecodeWorkload
+    wl_cls = (MultiTokenWorkload if cfg.tokens > 1 else EncoderDecodeWorkload if cfg.group_caches
+              else DecodeWorkload)
     wl = wl_cls(cfg, dev, seed=1234 + 7919 * rank, batch=args.batch, pool_rule=args.pool_rule)
     G = len(cfg.groups)
     flush = L2Flush(dev)
@@ -707,11 +830,15 @@ def run_csa2(args, world, rank, local):
 class OracleSample:
     """One decode step of ONE sequence of the config, run by the oracle.
 
-    Inputs are generated once (untimed); step() is the timed part: the new
-    token's FP4 append, the group's indexer over every position (Full) or
-    block means + pool + Reindex, Top-512, and each layer's attention. The
-    FP4 rows a step reads are quantised by the oracle inside the step from
-    their bf16 source rows (the oracle keeps no FP4 cache of its own)."""
+    Inputs are generated once (untimed). step() is the timed part: the new
+    entry's FP4 append, then every layer group of the config in order:
+    - the indexer over every position (Full) or block means + pool + Reindex;
+    - Top-512;
+    - each of the group's layers' attention.
+    Groups share one cache, or each Full group has its own when the config
+    says so. The FP4 rows a step reads are quantised by the oracle inside the
+    step from their bf16 source rows (the oracle keeps no FP4 cache of its
+    own)."""
 
     def __init__(self, cfg, seed=99):
         import numpy as np
@@ -719,43 +846,61 @@ class OracleSample:
         import synth
         self.cfg = cfg
         n, d_I, H_I, H = cfg.n, cfg.d_I, cfg.H_I, cfg.H
-        self.kI = synth.indexer_keys_e4m3((n, d_I), seed, bias_prob=cfg.bias_prob).numpy()
-        chunk = 1 << 16
-        self.kv = np.empty((n, 512), dtype=np.uint16)
-        for c0 in range(0, n, chunk):
-            r = min(chunk, n - c0)
-            self.kv[c0:c0 + r] = synth.normal_bf16((r, 512), seed, "kv", sub=c0 // chunk).view(torch.int16).numpy().view(np.uint16)
-        self.L = 1 + cfg.groups[0][1]
+        G = len(cfg.groups)
+        n_caches = G if cfg.group_caches else 1
         bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
-        self.q = [bits(synth.normal_bf16((H, 512), seed, "q", sub=l)) for l in range(self.L)]
-        self.swa = [bits(synth.normal_bf16((cfg.W, 512), seed, "swa", sub=l)) for l in range(self.L)]
-        self.qI = synth.normal_e4m3((H_I, d_I), seed, "qI").numpy()
-        self.w = synth.uniform_f32((H_I,), seed, "w").numpy()
-        self.codes = np.zeros((n, 256), dtype=np.uint8)
-        self.scales = np.zeros((n, 32), dtype=np.uint8)
-        mode = cfg.groups[0][0]
-        self.desc = (f"one sequence (batch 1) of the {cfg.workload} step: FP4 append, "
-                     f"{'Full scan of all ' + str(n) + ' positions' if mode == 'full' else 'block means + pool + Reindex'}, "
-                     f"Top-{cfg.k}, {self.L} attention layers; gathered rows quantised inside the step"
+        self.kI, self.kv = [], []
+        chunk = 1 << 16
+        for c in range(n_caches):
+            self.kI.append(synth.indexer_keys_e4m3((n, d_I), seed, bias_prob=cfg.bias_prob, sub=c).numpy())
+            kv = np.empty((n, 512), dtype=np.uint16)
+            for c0 in range(0, n, chunk):
+                r = min(chunk, n - c0)
+                kv[c0:c0 + r] = bits(synth.normal_bf16((r, 512), seed, "kv", sub=c * 4096 + c0 // chunk))
+            self.kv.append(kv)
+        self.layers = sum(1 + g[1] for g in cfg.groups)
+        self.q = [bits(synth.normal_bf16((H, 512), seed, "q", sub=l)) for l in range(self.layers)]
+        self.swa = [bits(synth.normal_bf16((cfg.W, 512), seed, "swa", sub=l)) for l in range(self.layers)]
+        self.qI = [synth.normal_e4m3((H_I, d_I), seed, "qI", sub=g).numpy() for g in range(G)]
+        self.w = [synth.uniform_f32((H_I,), seed, "w", sub=g).numpy() for g in range(G)]
+        self.qI_pool = synth.normal_e4m3((H_I, d_I), seed, "qI_pool").numpy()
+        self.w_pool = synth.uniform_f32((H_I,), seed, "w_pool").numpy()
+        self.codes = [np.zeros((n, 256), dtype=np.uint8) for _ in range(n_caches)]
+        self.scales = [np.zeros((n, 32), dtype=np.uint8) for _ in range(n_caches)]
+        parts = []
+        for mode, n_reuse, form_pool in cfg.groups:
+            first = f"Full scan of all {n} positions" if mode == "full" else "Reindex over the pool"
+            parts.append(first + (" + pool" if form_pool else "") + f", Top-{cfg.k}, {1 + n_reuse} attention layers")
+        self.desc = (f"one sequence (batch 1) of the {cfg.workload} step: FP4 append, then "
+                     + "; ".join(parts)
+                     + ("; separate caches per group" if cfg.group_caches else "")
+                     + "; gathered rows quantised inside the step"
                      + (f"; one of the {cfg.tokens} new tokens of a multi-token step (each costs the same)"
                         if cfg.tokens > 1 else ""))
 
     def step(self):
-        import numpy as np
         import oracle
         cfg, n = self.cfg, self.cfg.n
         t0 = time.perf_counter()
-        oracle.quantize_fp4(self.kv[n - 1:n])
-        if cfg.groups[0][0] == "full":
-            idx, _ = oracle.full_topk(self.qI, self.w, self.kI, n, cfg.k)
-        else:
-            kbar = oracle.block_means(self.kI, n)
-            pool, _ = oracle.form_pool(self.qI, self.w, kbar, cfg.P)
-            idx, _, _ = oracle.reindex_topk(self.qI, self.w, self.kI, pool, n, cfg.k)
-        rows = idx[idx >= 0]
-        self.codes[rows], self.scales[rows] = oracle.quantize_fp4(self.kv[rows])
-        for l in range(self.L):
-            oracle.sparse_attention(self.q[l], self.codes, self.scales, idx, self.swa[l], cfg.W)
+        for kv in self.kv:
+            oracle.quantize_fp4(kv[n - 1:n])
+        pool, l0 = None, 0
+        for g, (mode, n_reuse, form_pool) in enumerate(cfg.groups):
+            c = g if cfg.group_caches else 0
+            kI = self.kI[c]
+            if mode == "full":
+                idx, _ = oracle.full_topk(self.qI[g], self.w[g], kI, n, cfg.k)
+                if form_pool:
+                    pool, _ = oracle.form_pool(self.qI[g], self.w[g], oracle.block_means(kI, n), cfg.P)
+            else:
+                if form_pool or pool is None:
+                    pool, _ = oracle.form_pool(self.qI_pool, self.w_pool, oracle.block_means(kI, n), cfg.P)
+                idx, _, _ = oracle.reindex_topk(self.qI[g], self.w[g], kI, pool, n, cfg.k)
+            rows = idx[idx >= 0]
+            self.codes[c][rows], self.scales[c][rows] = oracle.quantize_fp4(self.kv[c][rows])
+            for l in range(l0, l0 + 1 + n_reuse):
+                oracle.sparse_attention(self.q[l], self.codes[c], self.scales[c], idx, self.swa[l], cfg.W)
+            l0 += 1 + n_reuse
         return time.perf_counter() - t0
 
 

@@ -28,7 +28,8 @@ EXPORTS = (
     "csa2_quantize_kv_fp4", "csa2_append_indexer_k", "csa2_block_means", "csa2_append_swa",
     "csa2_index_scores", "csa2_topk", "csa2_index_full", "csa2_form_pool", "csa2_form_pool_block_max",
     "csa2_index_reindex",
-    "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_prefill_index_scores",
+    "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_append_step_ratio",
+    "csa2_prefill_index_scores",
     "csa2_prefill_group",
 )
 
@@ -101,6 +102,9 @@ def lib() -> ctypes.CDLL:
     L.csa2_prefill_group.argtypes = [ctypes.POINTER(PrefillArgs), _c_p]
     L.csa2_append_step.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32,
                                    _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p]
+    L.csa2_append_step_ratio.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32,
+                                         _c_i32, _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_i64,
+                                         _c_p, _c_p, _c_p, _c_p]
     for name in EXPORTS:
         if name not in ("csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size"):
             getattr(L, name).restype = ctypes.c_int
@@ -231,6 +235,38 @@ def csa2_append_step(kv_new, kI_new, swa_new: Sequence[torch.Tensor], swa: Seque
                                 _ptr(codes), _ptr(scales), _ptr(kI), _ptr(kbar), codes.shape[1], _ptr(d_status),
                                 _stream(stream))
     _check(rc, "csa2_append_step")
+
+
+def csa2_append_step_ratio(kv_new, kI_new, swa_new: Sequence[torch.Tensor], swa: Sequence[torch.Tensor], pos, ratio,
+                           codes, scales, kI, kbar=None, n_vis_out=None, swa_len_out=None, d_status=None,
+                           stream=None):
+    """One token at compression ratio `ratio`: every layer's SWA row at slot pos % W; the
+    compressed entry (kv_new [B][512] bf16, kI_new [B][d_I]) only when it completes at this
+    token, at entry index (pos + 1) / ratio - 1. Optionally writes the visible entry count
+    n_vis_out [B] int64 and swa_len_out [B] int32."""
+    _need(kv_new, "kv_new", torch.bfloat16, 2)
+    _need(kI_new, "kI_new", torch.uint8, 2)
+    _need(pos, "pos", torch.int64, 1)
+    _need(codes, "codes", torch.uint8, 3)
+    _need(scales, "scales", torch.uint8, 3)
+    _need(kI, "kI", torch.uint8, 3)
+    _opt(kbar, "kbar", torch.uint8, 3)
+    _opt(n_vis_out, "n_vis_out", torch.int64, 1)
+    _opt(swa_len_out, "swa_len_out", torch.int32, 1)
+    L = len(swa_new)
+    if len(swa) != L:
+        raise ValueError("swa_new and swa must have the same length")
+    for i in range(L):
+        _need(swa_new[i], f"swa_new[{i}]", torch.bfloat16, 2)
+        _need(swa[i], f"swa[{i}]", torch.bfloat16, 3)
+    B, d = kv_new.shape
+    W = swa[0].shape[1] if L else 128
+    sn = (_c_p * max(L, 1))(*[t.data_ptr() for t in swa_new])
+    sw = (_c_p * max(L, 1))(*[t.data_ptr() for t in swa])
+    rc = lib().csa2_append_step_ratio(_ptr(kv_new), _ptr(kI_new), sn, sw, L, W, B, d, kI_new.shape[1], _ptr(pos),
+                                      int(ratio), _ptr(codes), _ptr(scales), _ptr(kI), _ptr(kbar), codes.shape[1],
+                                      _ptr(n_vis_out), _ptr(swa_len_out), _ptr(d_status), _stream(stream))
+    _check(rc, "csa2_append_step_ratio")
 
 
 def csa2_index_scores(qI, w, kI, n, n_max, scores, kI_seq_stride=None, d_status=None, stream=None):

@@ -28,8 +28,9 @@ int launch_block_means(const uint8_t* kI, int B, int d_I, const int64_t* n, int6
 int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa, int W,
                       cudaStream_t s);
 int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
-                       int L, int W, int B, int d_I, const int64_t* pos, uint8_t* codes, uint8_t* scales,
-                       uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st, cudaStream_t s);
+                       int L, int W, int B, int d_I, const int64_t* pos, int ratio, uint8_t* codes,
+                       uint8_t* scales, uint8_t* kI, uint8_t* kbar, int64_t n_cap, int64_t* n_vis_out,
+                       int32_t* swa_len_out, int32_t* st, cudaStream_t s);
 int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride, int rps,
                       const int64_t* n, int len_div, int B, int H_I, int d_I, int64_t n_max, float* scores,
                       int64_t scores_stride, const int32_t* pool, int P, int32_t* cand_pos,
@@ -261,7 +262,16 @@ int csa2_append_step(const void* kv_new, const uint8_t* kI_new, const void* cons
                      int32_t L, int32_t W, int32_t B, int32_t d, int32_t d_I, const int64_t* pos,
                      uint8_t* codes, uint8_t* scales, uint8_t* kI, uint8_t* kbar, int64_t n_cap,
                      int32_t* d_status, void* stream) {
-  if (B < 0 || L < 0 || n_cap < 0 || (L > 0 && W <= 0)) return CSA2_ERR_INVALID_ARG;
+  return csa2_append_step_ratio(kv_new, kI_new, swa_new, swa, L, W, B, d, d_I, pos, 1, codes, scales, kI, kbar,
+                                n_cap, nullptr, nullptr, d_status, stream);
+}
+
+int csa2_append_step_ratio(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new,
+                           void* const* swa, int32_t L, int32_t W, int32_t B, int32_t d, int32_t d_I,
+                           const int64_t* pos, int32_t ratio, uint8_t* codes, uint8_t* scales, uint8_t* kI,
+                           uint8_t* kbar, int64_t n_cap, int64_t* n_vis_out, int32_t* swa_len_out,
+                           int32_t* d_status, void* stream) {
+  if (B < 0 || L < 0 || n_cap < 0 || (L > 0 && W <= 0) || ratio < 1) return CSA2_ERR_INVALID_ARG;
   if (d != 512 || (d_I != 64 && d_I != 128) || L > 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (B == 0) return CSA2_OK;
   if (!kv_new || !kI_new || !pos || !codes || !scales || !kI || (L > 0 && (!swa_new || !swa)))
@@ -271,8 +281,9 @@ int csa2_append_step(const void* kv_new, const uint8_t* kI_new, const void* cons
     return CSA2_ERR_INVALID_ARG;
   for (int l = 0; l < L; ++l)
     if (!swa_new[l] || !swa[l] || !aligned16(swa_new[l]) || !aligned16(swa[l])) return CSA2_ERR_INVALID_ARG;
-  return launch_append_step(kv_new, kI_new, swa_new, swa, L, W, B, d_I, pos, codes, scales, kI, kbar, n_cap,
-                            d_status, static_cast<cudaStream_t>(stream));
+  if (swa_len_out && W <= 0) return CSA2_ERR_INVALID_ARG;
+  return launch_append_step(kv_new, kI_new, swa_new, swa, L, W, B, d_I, pos, ratio, codes, scales, kI, kbar, n_cap,
+                            n_vis_out, swa_len_out, d_status, static_cast<cudaStream_t>(stream));
 }
 
 int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,

@@ -175,30 +175,48 @@ struct StepLayers {
   uint4* dst[kMaxStepLayers];         // [B][W][d] bf16 rings
 };
 
-// One warp per task; task = b * (2 + L) + kind: kind 0 quantises the main-KV
-// row, kind 1 appends the indexer key and refreshes its block mean (the new
-// key is taken from the input, the block's earlier keys from the cache),
-// kind 2 + l writes layer l's SWA row into slot pos % W.
+// One warp per task; task = b * (2 + L) + kind. pos[b] is the new token's
+// position tok; `ratio` tokens make one compressed main-KV entry, which is
+// complete (and appended, at entry index (tok + 1) / ratio - 1) only when
+// (tok + 1) % ratio == 0. Kind 0 quantises the entry's main-KV row (and writes
+// the token's visible entry count and SWA length when asked), kind 1 appends
+// its indexer key and refreshes the block mean (the new key is taken from
+// the input, the block's earlier keys from the cache), kind 2 + l writes
+// layer l's SWA row into slot tok % W.
 __global__ void __launch_bounds__(256) k_append_step(const uint4* __restrict__ kv_new,
                                                      const uint8_t* __restrict__ kI_new, StepLayers layers,
                                                      int L, int W, int B, int d_I,
-                                                     const int64_t* __restrict__ pos, uint8_t* __restrict__ codes,
+                                                     const int64_t* __restrict__ pos, int ratio,
+                                                     uint8_t* __restrict__ codes,
                                                      uint8_t* __restrict__ scales, uint8_t* __restrict__ kI,
-                                                     uint8_t* __restrict__ kbar, int64_t n_cap, int32_t* st) {
+                                                     uint8_t* __restrict__ kbar, int64_t n_cap,
+                                                     int64_t* __restrict__ n_vis_out,
+                                                     int32_t* __restrict__ swa_len_out, int32_t* st) {
   const int lane = threadIdx.x & 31;
   const int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int per = 2 + L;
   if (task >= (int64_t)B * per) return;
   const int b = (int)(task / per), kind = (int)(task - (int64_t)b * per);
-  const int64_t p = pos[b];
-  if (p < 0 || p >= n_cap) {
+  const int64_t tok = pos[b];
+  if (tok < 0) {
+    if (lane == 0 && kind == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (kind == 0 && lane == 0) {
+    if (n_vis_out) n_vis_out[b] = (tok + 1) / ratio;
+    if (swa_len_out) swa_len_out[b] = (int32_t)(tok + 1 < W ? tok + 1 : W);
+  }
+  const int64_t p = (tok + 1) % ratio == 0 ? (tok + 1) / ratio - 1 : -1;   // entry index, or none this token
+  if (kind < 2 && p >= n_cap) {
     if (lane == 0 && kind == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
     return;
   }
   if (kind == 0) {
+    if (p < 0) return;
     const int64_t row = (int64_t)b * n_cap + p;
     quantize_row_warp(kv_new + (int64_t)b * 64, codes + row * 256, scales + row * 32, lane);
   } else if (kind == 1) {
+    if (p < 0) return;
     const uint8_t* kseq = kI + (int64_t)b * n_cap * d_I;
     const int c = lane * 4;
     if (c < d_I) {
@@ -223,7 +241,7 @@ __global__ void __launch_bounds__(256) k_append_step(const uint4* __restrict__ k
     }
   } else {
     const int l = kind - 2;
-    const int64_t slot = p % W;
+    const int64_t slot = tok % W;
     const uint4* src = layers.src[l] + (int64_t)b * 64;
     uint4* dst = layers.dst[l] + ((int64_t)b * W + slot) * 64;
     dst[lane] = src[lane];
@@ -286,8 +304,9 @@ int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa
 
 namespace csa2 {
 int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
-                       int L, int W, int B, int d_I, const int64_t* pos, uint8_t* codes, uint8_t* scales,
-                       uint8_t* kI, uint8_t* kbar, int64_t n_cap, int32_t* st, cudaStream_t s) {
+                       int L, int W, int B, int d_I, const int64_t* pos, int ratio, uint8_t* codes,
+                       uint8_t* scales, uint8_t* kI, uint8_t* kbar, int64_t n_cap, int64_t* n_vis_out,
+                       int32_t* swa_len_out, int32_t* st, cudaStream_t s) {
   if (L > kMaxStepLayers) return CSA2_ERR_UNSUPPORTED_SHAPE;
   StepLayers ly;
   for (int l = 0; l < kMaxStepLayers; ++l) {
@@ -296,7 +315,8 @@ int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* co
   }
   const int64_t warps = (int64_t)B * (2 + L);
   k_append_step<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(reinterpret_cast<const uint4*>(kv_new), kI_new, ly, L,
-                                                            W, B, d_I, pos, codes, scales, kI, kbar, n_cap, st);
+                                                            W > 0 ? W : 1, B, d_I, pos, ratio, codes, scales, kI,
+                                                            kbar, n_cap, n_vis_out, swa_len_out, st);
   count_launch();
   return launch_status();
 }

@@ -152,6 +152,25 @@ CSA2_API int csa2_append_step(const void* kv_new, const uint8_t* kI_new,
                               uint8_t* scales, uint8_t* kI, uint8_t* kbar,
                               int64_t n_cap, int32_t* d_status, void* stream);
 
+/* Encoder-style append at compression ratio `ratio` (tokens per compressed
+ * main-KV entry; ratio 1 is csa2_append_step). pos[b] is the new token's
+ * position t. Every call writes each layer's SWA row into slot t % W. The
+ * compressed entry (kv_new, kI_new: an input, since merging tokens into an
+ * entry needs weights) is appended, with its block mean refreshed, only
+ * when it completes at this token: at entry index (t + 1) / ratio - 1 when
+ * (t + 1) % ratio == 0 (checked per sequence on the device, so the launch is
+ * the same every step). When not NULL, n_vis_out[b] = (t + 1) / ratio (the
+ * entries the token sees) and swa_len_out[b] = min(t + 1, W) are written.
+ * Arrays as in csa2_append_step. */
+CSA2_API int csa2_append_step_ratio(const void* kv_new, const uint8_t* kI_new,
+                                    const void* const* swa_new, void* const* swa,
+                                    int32_t L, int32_t W, int32_t B, int32_t d,
+                                    int32_t d_I, const int64_t* pos, int32_t ratio,
+                                    uint8_t* codes, uint8_t* scales, uint8_t* kI,
+                                    uint8_t* kbar, int64_t n_cap, int64_t* n_vis_out,
+                                    int32_t* swa_len_out, int32_t* d_status,
+                                    void* stream);
+
 /* ---- a3: indexer scores [CSA2] ------------------------------------------ */
 /* Raw indexer scan: scores[b][t] = sum_h w[b][h] * relu(qI[b][h] . kI[b][t])
  * for t < n[b], FP8 x FP8 products accumulated in fp32 on the tensor cores

@@ -29,6 +29,7 @@ class Config:
     prefill_queries: int = 0
     ratio: int = 1         # compression ratio (tokens per main-KV entry)
     tokens: int = 1        # new tokens per sequence and step (multi-token decode)
+    group_caches: bool = False   # each Full group keeps its own caches (the encoder's groups)
     extra: dict = field(default_factory=dict)
 
 
@@ -46,6 +47,12 @@ CONFIGS = {
               groups=(("full", 3, True),) + (("reindex", 3, False),) * 4),
     6: Config("cfg6", "decoder_group_full3reuse_b32x4tok_ctx131072", B=32, n=131072, bias_prob=0.05,
               groups=(("full", 3, False),), tokens=4),
+    # the encoder's 18 layers: 3 groups of Full + 5 Reuse at ratio 2, each group
+    # with its own main KV and indexer K (n = entries at the end)
+    7: Config("cfg7", "encoder_stack18_ratio2_decode_b4_ctx262144_256steps", B=4, n=131072, ratio=2, steps=256,
+              groups=(("full", 5, False),) * 3, group_caches=True),
+    8: Config("cfg8", "encoder_stack18_prefill_chunk4096_ratio2_ctx262144", B=1, n=131072, prefill_queries=4096,
+              ratio=2, groups=(("full", 5, False),) * 3, group_caches=True),
 }
 
 
