@@ -29,6 +29,7 @@ EXPORTS = (
     "csa2_index_scores", "csa2_topk", "csa2_index_full", "csa2_form_pool", "csa2_form_pool_block_max",
     "csa2_index_reindex",
     "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_append_step_ratio",
+    "csa2_swa_export", "csa2_swa_restore",
     "csa2_prefill_index_scores",
     "csa2_prefill_group",
 )
@@ -102,6 +103,9 @@ def lib() -> ctypes.CDLL:
     L.csa2_prefill_group.argtypes = [ctypes.POINTER(PrefillArgs), _c_p]
     L.csa2_append_step.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32,
                                    _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p]
+    L.csa2_swa_export.argtypes = [ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32, _c_i32, _c_p, ctypes.POINTER(_c_p), _c_p]
+    L.csa2_swa_restore.argtypes = [ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32, _c_i32, _c_p, ctypes.POINTER(_c_p),
+                                   _c_p, _c_p]
     L.csa2_append_step_ratio.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32,
                                          _c_i32, _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_i64,
                                          _c_p, _c_p, _c_p, _c_p]
@@ -267,6 +271,32 @@ def csa2_append_step_ratio(kv_new, kI_new, swa_new: Sequence[torch.Tensor], swa:
                                       int(ratio), _ptr(codes), _ptr(scales), _ptr(kI), _ptr(kbar), codes.shape[1],
                                       _ptr(n_vis_out), _ptr(swa_len_out), _ptr(d_status), _stream(stream))
     _check(rc, "csa2_append_step_ratio")
+
+
+def _swa_lists(a, b, n):
+    _need(n, "n", torch.int64, 1)
+    if len(a) != len(b) or not a:
+        raise ValueError("one array per layer on both sides")
+    for i in range(len(a)):
+        _need(a[i], f"layer {i}", torch.bfloat16, 3)
+        _need(b[i], f"layer {i}", torch.bfloat16, 3)
+    L = len(a)
+    B, W, d = a[0].shape
+    return L, W, B, d, (_c_p * L)(*[t.data_ptr() for t in a]), (_c_p * L)(*[t.data_ptr() for t in b])
+
+
+def csa2_swa_export(rings, n, rows_out, stream=None):
+    """Each layer's window in token order: rows_out[l][b][i] = token n[b]-c+i (c = min(n[b], W))."""
+    L, W, B, d, pa, pb = _swa_lists(rings, rows_out, n)
+    _check(lib().csa2_swa_export(pa, L, W, B, d, _ptr(n), pb, _stream(stream)), "csa2_swa_export")
+
+
+def csa2_swa_restore(rows, n, rings, swa_len_out=None, stream=None):
+    """Write token-ordered window rows back into each layer's ring (token t at slot t % W)."""
+    _opt(swa_len_out, "swa_len_out", torch.int32, 1)
+    L, W, B, d, pa, pb = _swa_lists(rows, rings, n)
+    _check(lib().csa2_swa_restore(pa, L, W, B, d, _ptr(n), pb, _ptr(swa_len_out), _stream(stream)),
+           "csa2_swa_restore")
 
 
 def csa2_index_scores(qI, w, kI, n, n_max, scores, kI_seq_stride=None, d_status=None, stream=None):

@@ -27,6 +27,8 @@ int launch_block_means(const uint8_t* kI, int B, int d_I, const int64_t* n, int6
                        int64_t n_cap, uint8_t* kbar, int32_t* st, cudaStream_t s);
 int launch_append_swa(const void* x, int B, int d, const int64_t* pos, void* swa, int W,
                       cudaStream_t s);
+int launch_swa_ring(const void* const* src, void* const* dst, int L, int W, int B, int d, const int64_t* n,
+                    int to_ring, int32_t* swa_len_out, cudaStream_t s);
 int launch_append_step(const void* kv_new, const uint8_t* kI_new, const void* const* swa_new, void* const* swa,
                        int L, int W, int B, int d_I, const int64_t* pos, int ratio, uint8_t* codes,
                        uint8_t* scales, uint8_t* kI, uint8_t* kbar, int64_t n_cap, int64_t* n_vis_out,
@@ -284,6 +286,30 @@ int csa2_append_step_ratio(const void* kv_new, const uint8_t* kI_new, const void
   if (swa_len_out && W <= 0) return CSA2_ERR_INVALID_ARG;
   return launch_append_step(kv_new, kI_new, swa_new, swa, L, W, B, d_I, pos, ratio, codes, scales, kI, kbar, n_cap,
                             n_vis_out, swa_len_out, d_status, static_cast<cudaStream_t>(stream));
+}
+
+static int swa_ring_args(const void* const* a, const void* const* b, int32_t L, int32_t W, int32_t B, int32_t d,
+                         const int64_t* n) {
+  if (L < 0 || W <= 0 || B < 0) return CSA2_ERR_INVALID_ARG;
+  if (d != 512 || L > 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (L > 0 && B > 0 && (!a || !b || !n)) return CSA2_ERR_INVALID_ARG;
+  for (int l = 0; l < L && B > 0; ++l)
+    if (!a[l] || !b[l] || !aligned16(a[l]) || !aligned16(b[l])) return CSA2_ERR_INVALID_ARG;
+  return CSA2_OK;
+}
+
+int csa2_swa_export(const void* const* rings, int32_t L, int32_t W, int32_t B, int32_t d, const int64_t* n,
+                    void* const* rows_out, void* stream) {
+  const int rc = swa_ring_args(rings, rows_out, L, W, B, d, n);
+  if (rc != CSA2_OK || L == 0 || B == 0) return rc;
+  return launch_swa_ring(rings, rows_out, L, W, B, d, n, 0, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int csa2_swa_restore(const void* const* rows, int32_t L, int32_t W, int32_t B, int32_t d, const int64_t* n,
+                     void* const* rings, int32_t* swa_len_out, void* stream) {
+  const int rc = swa_ring_args(rows, rings, L, W, B, d, n);
+  if (rc != CSA2_OK || L == 0 || B == 0) return rc;
+  return launch_swa_ring(rows, rings, L, W, B, d, n, 1, swa_len_out, static_cast<cudaStream_t>(stream));
 }
 
 int csa2_index_scores(const uint8_t* qI, const float* w, const uint8_t* kI, int64_t kI_seq_stride,

@@ -249,6 +249,38 @@ __global__ void __launch_bounds__(256) k_append_step(const uint4* __restrict__ k
   }
 }
 
+// ---- SWA ring <-> token order (buffer management for a restored session) ----
+// A layer's ring holds token t of sequence b at slot t % W. After n[b] tokens
+// the window is tokens n - c .. n - 1, c = min(n, W). to_ring = 0 (export):
+// lin[b][i] = ring row of token n - c + i for i < c, zero rows after it.
+// to_ring = 1 (restore): each lin[b][i], i < c, goes to its token's slot and
+// swa_len_out[b] = c. One warp per (layer, sequence, row).
+__global__ void __launch_bounds__(256) k_swa_ring(StepLayers layers, int L, int W, int B, int chunks,
+                                                  const int64_t* __restrict__ n, int to_ring,
+                                                  int32_t* __restrict__ swa_len_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t task = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (task >= (int64_t)L * B * W) return;
+  const int l = (int)(task / ((int64_t)B * W));
+  const int64_t rem = task - (int64_t)l * B * W;
+  const int b = (int)(rem / W), i = (int)(rem - (int64_t)b * W);
+  const int64_t nb = n[b] > 0 ? n[b] : 0;
+  const int64_t c = nb < W ? nb : W;
+  const int64_t slot = (nb - c + i) % W;
+  const uint4* src = layers.src[l];
+  uint4* dst = layers.dst[l];
+  if (to_ring) {
+    if (i < c)
+      for (int x = lane; x < chunks; x += 32)
+        dst[((int64_t)b * W + slot) * chunks + x] = src[((int64_t)b * W + i) * chunks + x];
+    if (swa_len_out && l == 0 && i == 0 && lane == 0) swa_len_out[b] = (int32_t)c;
+  } else {
+    for (int x = lane; x < chunks; x += 32)
+      dst[((int64_t)b * W + i) * chunks + x] =
+          i < c ? src[((int64_t)b * W + slot) * chunks + x] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // ---- host launchers -----------------------------------------------------
 int launch_quantize_fp4(const void* x, int B, int64_t rows, const int64_t* pos, uint8_t* codes,
                         uint8_t* scales, int64_t n_cap, int32_t* st, cudaStream_t s) {
@@ -287,6 +319,21 @@ int launch_block_means(const uint8_t* kI, int B, int d_I, const int64_t* n, int6
   if (nb == 0 || B == 0) return CSA2_OK;
   dim3 grid((unsigned)((nb + 7) / 8), (unsigned)B);
   k_block_means_all<<<grid, 256, 0, s>>>(kI, d_I, n, n_cap, kbar, st);
+  count_launch();
+  return launch_status();
+}
+
+int launch_swa_ring(const void* const* src, void* const* dst, int L, int W, int B, int d, const int64_t* n,
+                    int to_ring, int32_t* swa_len_out, cudaStream_t s) {
+  if (L > kMaxStepLayers) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  StepLayers ly;
+  for (int l = 0; l < kMaxStepLayers; ++l) {
+    ly.src[l] = l < L ? reinterpret_cast<const uint4*>(src[l]) : nullptr;
+    ly.dst[l] = l < L ? reinterpret_cast<uint4*>(dst[l]) : nullptr;
+  }
+  const int64_t warps = (int64_t)L * B * W;
+  if (warps == 0) return CSA2_OK;
+  k_swa_ring<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(ly, L, W, B, d / 8, n, to_ring, swa_len_out);
   count_launch();
   return launch_status();
 }

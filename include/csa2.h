@@ -138,6 +138,24 @@ CSA2_API int csa2_block_means(const uint8_t* kI, int32_t B, int32_t d_I,
 CSA2_API int csa2_append_swa(const void* x, int32_t B, int32_t d, const int64_t* pos,
                     void* swa, int32_t W, void* stream);
 
+/* Sliding-window rings and token order [CED]. Each layer keeps the last W
+ * tokens' rows in a ring: token t of sequence b at slot t mod W. After n[b]
+ * tokens the window is tokens n - c .. n - 1, c = min(n[b], W).
+ * csa2_swa_export copies every layer's window out in token order:
+ * rows_out[l][b][i] = the row of token n - c + i for i < c, zero rows after.
+ * csa2_swa_restore writes rows given in that order back into their slots
+ * (the buffer side of restoring a session whose window rows were saved or
+ * recomputed; the recomputation itself needs weights and is not here) and,
+ * if swa_len_out is not NULL, sets swa_len_out[b] = c.
+ *   rings, rows  HOST arrays [L] of device [B][W][d] bf16; n [B] int64 device.
+ *   d = 512, L <= 64. */
+CSA2_API int csa2_swa_export(const void* const* rings, int32_t L, int32_t W, int32_t B,
+                             int32_t d, const int64_t* n, void* const* rows_out,
+                             void* stream);
+CSA2_API int csa2_swa_restore(const void* const* rows, int32_t L, int32_t W, int32_t B,
+                              int32_t d, const int64_t* n, void* const* rings,
+                              int32_t* swa_len_out, void* stream);
+
 /* Append one decode token to every cache of a layer stack in ONE launch:
  * the main-KV row x_b (FP4, exactly as csa2_quantize_kv_fp4), the indexer
  * key (with its block mean, exactly as csa2_append_indexer_k; kbar may be

@@ -63,13 +63,14 @@ from .csa2 import (
     sparse_attention,
     layer_group,
     prefill_visible,
+    swa_ring_after,
     prefill_swa_rows,
 )
 
 __all__ = [
     "E2M1_GRID", "E4M3_MAX", "bf16_bits_to_f64", "e4m3_decode", "e4m3_encode",
     "e2m1_encode_mag", "quantize_fp4", "dequant_fp4", "indexer_scores",
-    "block_means", "topk_select", "full_topk", "form_pool", "pool_positions",
-    "reindex_topk", "sparse_attention", "layer_group", "prefill_visible",
-    "prefill_swa_rows",
+    "block_means", "topk_select", "full_topk", "form_pool", "form_pool_block_max",
+    "pool_positions", "reindex_topk", "sparse_attention", "layer_group", "prefill_visible",
+    "prefill_swa_rows", "swa_ring_after",
 ]

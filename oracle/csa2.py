@@ -227,6 +227,20 @@ def layer_group(mode, q_layers, swa_layers, swa_len, codes, scales, n,
     return idx, outs
 
 
+def swa_ring_after(rows, n, W=128):
+    """The ring a layer holds after n tokens were appended one by one [CED].
+
+    [CED] keeps a 128-token sliding window in every layer; how it is stored is
+    the build's choice: a ring with token t at slot t mod W, rewritten by each
+    new token. rows [n][d] in token order -> ring [W][d] (slots of tokens not
+    yet seen are zero)."""
+    rows = np.asarray(rows)
+    ring = np.zeros((W,) + rows.shape[1:], dtype=rows.dtype)
+    for t in range(int(n)):
+        ring[t % W] = rows[t]
+    return ring
+
+
 # --------------------------------------------------------------------------
 # Prefill causal rule [CSA2] (encoder: compression ratio 2), [CED]
 # --------------------------------------------------------------------------

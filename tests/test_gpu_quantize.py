@@ -164,3 +164,37 @@ def test_append_step_matches_individual_appends(d_I, L):
     for i, p in enumerate(pos_list):
         ref = oracle.block_means(kI_np[i], p + 1)
         np.testing.assert_array_equal(u8(a[1])[i, p // 8], ref[p // 8])
+
+
+def test_swa_ring_export_and_restore():
+    """Rings filled by per-token appends: the export is the window in token
+    order (oracle), and restoring it into empty rings gives back the same
+    rings and window lengths."""
+    B, W, L = 3, 128, 2
+    n = np.array([300, 50, 128], dtype=np.int64)
+    rows = [synth.normal_bf16((B, int(n.max()), 512), seed=5, stream="swa", sub=l) for l in range(L)]
+    rings = [torch.zeros((B, W, 512), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    for t in range(int(n.max())):
+        live = torch.from_numpy((t < n).astype(np.int64)).to(DEV)
+        pos = torch.where(live > 0, torch.full_like(live, t), torch.full_like(live, -1))
+        for l in range(L):
+            for b in range(B):
+                if t < n[b]:
+                    csa2.csa2_append_swa(rows[l][b:b + 1, t].to(DEV), pos[b:b + 1], rings[l][b:b + 1])
+    n_d = torch.from_numpy(n).to(DEV)
+    out = [torch.full((B, W, 512), 7.0, dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    csa2.csa2_swa_export(rings, n_d, out)
+    back = [torch.zeros((B, W, 512), dtype=torch.bfloat16, device=DEV) for _ in range(L)]
+    swa_len = torch.zeros(B, dtype=torch.int32, device=DEV)
+    csa2.csa2_swa_restore(out, n_d, back, swa_len_out=swa_len)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(swa_len.cpu().numpy(), np.minimum(n, W))
+    for l in range(L):
+        ob, bb = bits16(out[l]), bits16(back[l])
+        for b in range(B):
+            c = min(int(n[b]), W)
+            window = bits16(rows[l])[b, int(n[b]) - c:int(n[b])]
+            np.testing.assert_array_equal(ob[b, :c], window)
+            assert (ob[b, c:] == 0).all()
+            np.testing.assert_array_equal(bb[b], oracle.swa_ring_after(bits16(rows[l])[b], int(n[b]), W))
+            np.testing.assert_array_equal(bits16(rings[l])[b], bb[b])

@@ -95,3 +95,20 @@ def test_reuse_equals_recompute_on_group_indices():
     np.testing.assert_array_equal(idx, full_idx)
     for l in range(L):
         np.testing.assert_array_equal(outs[l], oracle.sparse_attention(q[l], codes, scales, full_idx, swa[l], 128))
+
+
+def test_swa_ring_after_brute_force():
+    """The ring after n appends holds the last min(n, W) tokens, token t at
+    slot t mod W, against an explicit window of the last W tokens."""
+    rng = np.random.default_rng(3)
+    W = 16
+    rows = rng.integers(1, 1 << 15, (70, 4))
+    for n in (0, 1, 15, 16, 17, 40, 70):
+        ring = oracle.swa_ring_after(rows, n, W)
+        window = list(range(max(0, n - W), n))
+        for t in window:
+            assert (ring[t % W] == rows[t]).all()
+        filled = {t % W for t in window}
+        for slot in range(W):
+            if slot not in filled:
+                assert (ring[slot] == 0).all()
