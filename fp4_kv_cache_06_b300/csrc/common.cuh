@@ -166,6 +166,7 @@ __device__ __forceinline__ void topk_hist_flush(uint32_t* sh, uint32_t* __restri
   if (threadIdx.x == 0) {
     hdr->vbin = vbin;
     hdr->overflow = ge > (uint32_t)kCandCap ? 1u : 0u;
+    hdr->cnt = 0;            // a scan may have used it to hand out tiles; the compaction counts from 0
   }
 }
 

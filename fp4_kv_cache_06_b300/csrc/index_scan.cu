@@ -147,11 +147,17 @@ __global__ void __launch_bounds__(kScanThreads) k_index_scan(
 // by registers. Inside an m-tile, fragment row g reads smem row sigma(g) =
 // {0,4,1,5,2,6,3,7}[g] (and +8): with the swizzle this makes every 16-byte
 // shared load of a quarter-warp hit 8 distinct bank groups.
+// With a Top-K header the row's CTAs take tiles dynamically from the header's
+// counter (zero until the compaction, which the row's last CTA restores), so
+// a CTA on a slower SM simply takes fewer tiles; the producer passes each
+// tile's index to the consumers in shared memory and ends with index -1.
 constexpr int kTmaStages = 5;
 constexpr int kTmaRows = 128;
 constexpr int kTmaTile = kTmaRows * 128;          // 16 KB
 constexpr int kTmaThreads = 288;                  // 8 consumer warps + 1 producer warp
-constexpr int kTmaSmem = kTmaStages * kTmaTile + 1024 + 64;
+// after the tiles: full and empty barriers (2 x 8 x kTmaStages bytes), then the
+// stages' tile indices at +128; plus alignment slack
+constexpr int kTmaSmem = kTmaStages * kTmaTile + 1024 + 256;
 
 __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
     const __grid_constant__ CUtensorMap map_k, const uint8_t* __restrict__ qI, const float* __restrict__ w,
@@ -164,6 +170,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
   const uint32_t base = (raw + 1023) & ~1023u;
   unsigned char* sp = smem_raw + (base - raw);
   const uint32_t bar_full = base + kTmaStages * kTmaTile, bar_empty = bar_full + 8 * kTmaStages;
+  volatile int64_t* sTile = reinterpret_cast<volatile int64_t*>(sp + kTmaStages * kTmaTile + 128);  // [kTmaStages]
   const int b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
   const int64_t tiles_b = (nb + kTmaRows - 1) / kTmaRows;
   const int64_t t0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t t1 = min(t0 + (int64_t)tiles_per_cta, tiles_b);
-  const int nt = t1 > t0 ? (int)(t1 - t0) : 0;
+  const bool dynamic = hdr != nullptr;            // take tiles from the row's counter
 
   if (hist)
     for (int i = tid; i < kHistBins; i += kTmaThreads) sh_hist[i] = 0;
@@ -190,14 +197,24 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
   __syncthreads();
 
   if (warp == 8) {
-    if (lane == 0 && nt > 0) {                     // producer
+    if (lane == 0) {                               // producer
       tc::prefetch_tmap(&map_k);
-      for (int i = 0; i < nt; ++i) {
+      for (int i = 0;; ++i) {
         const int s = i % kTmaStages;
-        if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kTmaStages) & 1) ^ 1)) { report(st, CSA2_ERR_TIMEOUT); break; }
+        if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kTmaStages) & 1) ^ 1)) {
+          report(st, CSA2_ERR_TIMEOUT);            // the consumers time out on the full barrier
+          break;
+        }
+        const int64_t tile = dynamic ? (int64_t)atomicAdd(&hdr[b].cnt, 1u) : t0 + i;
+        if (tile >= (dynamic ? tiles_b : t1)) {
+          sTile[s] = -1;                           // no more tiles: an arrive without bytes
+          tc::mbar_arrive(bar_full + 8 * s);
+          break;
+        }
+        sTile[s] = tile;
         tc::mbar_expect_tx(bar_full + 8 * s, kTmaTile);
         tc::tma_load_2d(base + s * kTmaTile, &map_k, 0,
-                        (int32_t)((int64_t)(b / rps) * kI_seq_stride + (t0 + i) * kTmaRows), bar_full + 8 * s);
+                        (int32_t)((int64_t)(b / rps) * kI_seq_stride + tile * kTmaRows), bar_full + 8 * s);
       }
     }
   } else {                                         // consumers: warp w owns m-tile w of every tile
@@ -216,13 +233,15 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
     float* srow = scores + (int64_t)b * scores_stride;
     const int sg = ((g & 1) << 2) | (g >> 1);       // sigma(g)
     const int r1 = warp * 16 + sg, r2 = r1 + 8;     // tile rows of fragment rows g and g+8
-    for (int i = 0; i < nt; ++i) {
+    for (int i = 0;; ++i) {
       const int s = i % kTmaStages;
       const bool got = tc::mbar_wait(bar_full + 8 * s, (i / kTmaStages) & 1);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) report(st, CSA2_ERR_TIMEOUT);
         break;
       }
+      const int64_t tidx = sTile[s];               // read before the stage is released
+      if (tidx < 0) break;
       const unsigned char* tile = sp + s * kTmaTile;
       uint4 a[2][2];
 #pragma unroll
@@ -247,7 +266,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
       s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
       s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
       if (t < 2) {
-        const int64_t row = (t0 + i) * kTmaRows + (t ? r2 : r1);
+        const int64_t row = tidx * kTmaRows + (t ? r2 : r1);
         const float sc = t ? s1 : s0;
         if (row < nb) {
           srow[row] = sc;
