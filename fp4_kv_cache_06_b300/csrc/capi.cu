@@ -123,13 +123,17 @@ static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, in
   int rc;
   float* scores = scores_out ? scores_out : static_cast<float*>(ws);
   void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)n_max * 4);
-  if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
+  // several query rows per sequence: the scan reads each key tile once for
+  // all of them and writes plain scores; Top-K builds its own histogram
+  const bool shared_scan = rps == 2 || rps == 4 || rps == 8;
+  if (!shared_scan && (rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
   if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
   if ((rc = launch_index_scan(qI, w, kI, kI_seq_stride, rps, n, 1, B, H_I, d_I, n_max, scores, n_max, nullptr, 0,
-                              nullptr, topk_ws_hist(tk), topk_ws_hdr(tk, B), k, st, s)) != CSA2_OK)
+                              nullptr, shared_scan ? nullptr : topk_ws_hist(tk),
+                              shared_scan ? nullptr : topk_ws_hdr(tk, B), k, st, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
-  return launch_topk(scores, nullptr, n_max, n, 1, B, n_max, k, idx_out, tk, true, s);
+  return launch_topk(scores, nullptr, n_max, n, 1, B, n_max, k, idx_out, tk, !shared_scan, s);
 }
 
 static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, int64_t kbar_seq_stride, int rps,

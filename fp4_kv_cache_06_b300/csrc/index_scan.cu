@@ -159,6 +159,10 @@ constexpr int kTmaThreads = 288;                  // 8 consumer warps + 1 produc
 // stages' tile indices at +128; plus alignment slack
 constexpr int kTmaSmem = kTmaStages * kTmaTile + 1024 + 256;
 
+// R > 1: one CTA serves the R query rows of a sequence (multi-token decode):
+// every key tile is read once and scored against each row's queries; these
+// launches write plain scores (no histogram, static tile ranges).
+template <int R>
 __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
     const __grid_constant__ CUtensorMap map_k, const uint8_t* __restrict__ qI, const float* __restrict__ w,
     int64_t kI_seq_stride, int rps, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max, int tiles_per_cta,
@@ -171,21 +175,31 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
   unsigned char* sp = smem_raw + (base - raw);
   const uint32_t bar_full = base + kTmaStages * kTmaTile, bar_empty = bar_full + 8 * kTmaStages;
   volatile int64_t* sTile = reinterpret_cast<volatile int64_t*>(sp + kTmaStages * kTmaTile + 128);  // [kTmaStages]
-  const int b = blockIdx.y;
+  // R == 1: row b = blockIdx.y reads sequence b / rps; R > 1: rows
+  // R * blockIdx.y .. + R - 1 all read sequence blockIdx.y
+  const int b = R == 1 ? (int)blockIdx.y : (int)blockIdx.y * R;
+  const int64_t seq = R == 1 ? (int64_t)(b / rps) : (int64_t)blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
 
-  int64_t nb = n[b];
-  nb = nb < 0 ? nb : (nb + len_div - 1) / len_div;
-  if (nb > n_max || nb < 0) {
-    if (blockIdx.x == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
-    nb = nb < 0 ? 0 : n_max;
+  int64_t nr[R];                                  // visible rows (or blocks) of each row
+  int64_t nb = 0;                                 // the most any of them sees
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    int64_t v = n[b + r];
+    v = v < 0 ? v : (v + len_div - 1) / len_div;
+    if (v > n_max || v < 0) {
+      if (blockIdx.x == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
+      v = v < 0 ? 0 : n_max;
+    }
+    nr[r] = v;
+    nb = v > nb ? v : nb;
   }
   const int64_t tiles_b = (nb + kTmaRows - 1) / kTmaRows;
   const int64_t t0 = (int64_t)blockIdx.x * tiles_per_cta;
   const int64_t t1 = min(t0 + (int64_t)tiles_per_cta, tiles_b);
-  const bool dynamic = hdr != nullptr;            // take tiles from the row's counter
+  const bool dynamic = R == 1 && hdr != nullptr;  // take tiles from the row's counter
 
-  if (hist)
+  if (R == 1 && hist)
     for (int i = tid; i < kHistBins; i += kTmaThreads) sh_hist[i] = 0;
   if (tid == 0) {
     for (int i = 0; i < kTmaStages; ++i) {
@@ -214,23 +228,24 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
         sTile[s] = tile;
         tc::mbar_expect_tx(bar_full + 8 * s, kTmaTile);
         tc::tma_load_2d(base + s * kTmaTile, &map_k, 0,
-                        (int32_t)((int64_t)(b / rps) * kI_seq_stride + tile * kTmaRows), bar_full + 8 * s);
+                        (int32_t)(seq * kI_seq_stride + tile * kTmaRows), bar_full + 8 * s);
       }
     }
   } else {                                         // consumers: warp w owns m-tile w of every tile
-    uint32_t qf[8];
-    {
+    uint32_t qf[R][8];
+    float w0[R], w1[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
       const bool live = g < H_I;
-      const uint8_t* qrow = qI + ((int64_t)b * H_I + (live ? g : 0)) * 128;
+      const uint8_t* qrow = qI + ((int64_t)(b + r) * H_I + (live ? g : 0)) * 128;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const uint4 v = live ? *reinterpret_cast<const uint4*>(qrow + 64 * c + 16 * t) : make_uint4(0, 0, 0, 0);
-        qf[4 * c + 0] = v.x; qf[4 * c + 1] = v.y; qf[4 * c + 2] = v.z; qf[4 * c + 3] = v.w;
+        qf[r][4 * c + 0] = v.x; qf[r][4 * c + 1] = v.y; qf[r][4 * c + 2] = v.z; qf[r][4 * c + 3] = v.w;
       }
+      w0[r] = (2 * t < H_I) ? w[(int64_t)(b + r) * H_I + 2 * t] : 0.f;
+      w1[r] = (2 * t + 1 < H_I) ? w[(int64_t)(b + r) * H_I + 2 * t + 1] : 0.f;
     }
-    const float w0 = (2 * t < H_I) ? w[(int64_t)b * H_I + 2 * t] : 0.f;
-    const float w1 = (2 * t + 1 < H_I) ? w[(int64_t)b * H_I + 2 * t + 1] : 0.f;
-    float* srow = scores + (int64_t)b * scores_stride;
     const int sg = ((g & 1) << 2) | (g >> 1);       // sigma(g)
     const int r1 = warp * 16 + sg, r2 = r1 + 8;     // tile rows of fragment rows g and g+8
     for (int i = 0;; ++i) {
@@ -251,39 +266,43 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(bar_empty + 8 * s);   // this warp is done with the stage
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4& x0 = a[0][j >> 1];
-        const uint4& x1 = a[1][j >> 1];
-        mma_e4m3_16832(acc, (j & 1) ? x0.z : x0.x, (j & 1) ? x1.z : x1.x, (j & 1) ? x0.w : x0.y,
-                       (j & 1) ? x1.w : x1.y, qf[2 * j], qf[2 * j + 1]);
-      }
-      float s0 = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);
-      float s1 = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-      if (t < 2) {
-        const int64_t row = tidx * kTmaRows + (t ? r2 : r1);
-        const float sc = t ? s1 : s0;
-        if (row < nb) {
-          srow[row] = sc;
-          if (hist) atomicAdd(&sh_hist[score_key(sc) >> 20], 1u);
+      for (int r = 0; r < R; ++r) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4& x0 = a[0][j >> 1];
+          const uint4& x1 = a[1][j >> 1];
+          mma_e4m3_16832(acc, (j & 1) ? x0.z : x0.x, (j & 1) ? x1.z : x1.x, (j & 1) ? x0.w : x0.y,
+                         (j & 1) ? x1.w : x1.y, qf[r][2 * j], qf[r][2 * j + 1]);
+        }
+        float s0 = w0[r] * fmaxf(acc[0], 0.f) + w1[r] * fmaxf(acc[1], 0.f);
+        float s1 = w0[r] * fmaxf(acc[2], 0.f) + w1[r] * fmaxf(acc[3], 0.f);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        if (t < 2) {
+          const int64_t row = tidx * kTmaRows + (t ? r2 : r1);
+          const float sc = t ? s1 : s0;
+          if (row < nr[r]) {
+            scores[(int64_t)(b + r) * scores_stride + row] = sc;
+            if (R == 1 && hist) atomicAdd(&sh_hist[score_key(sc) >> 20], 1u);
+          }
         }
       }
     }
   }
-  if (hist) topk_hist_flush(sh_hist, hist + (int64_t)b * kHistBins, hdr + b, topk_k, gridDim.x);
+  if (R == 1 && hist) topk_hist_flush(sh_hist, hist + (int64_t)b * kHistBins, hdr + b, topk_k, gridDim.x);
 }
 
 bool make_tmap_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows);
 
 static int tma_scan_init = 0;
 int scan_init_attributes() {
-  if (cudaFuncSetAttribute(k_index_scan_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem) != cudaSuccess)
-    return CSA2_ERR_CUDA;
+  for (auto kern : {k_index_scan_tma<1>, k_index_scan_tma<2>, k_index_scan_tma<4>, k_index_scan_tma<8>})
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTmaSmem) != cudaSuccess)
+      return CSA2_ERR_CUDA;
   tma_scan_init = 1;
   return CSA2_OK;
 }
@@ -310,16 +329,25 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
     CUtensorMap map;
     if (make_tmap_rows128(&map, kI, total_rows, 128, kTmaRows)) {
       const int64_t tiles = (n_max + kTmaRows - 1) / kTmaRows;
-      // one wave of two CTAs per SM: each CTA streams a long contiguous run of
-      // tiles, so the ring is filled once per CTA
-      int64_t per_seq = (2 * kSMs) / B;
+      // rows of one sequence share a CTA (plain scores) when there are 2, 4 or 8
+      const int R = (hist == nullptr && (rps == 2 || rps == 4 || rps == 8)) ? rps : 1;
+      const int units = B / R;                      // CTA rows of the grid
+      // one wave of two CTAs per SM
+      int64_t per_seq = (2 * kSMs) / units;
       if (per_seq > tiles) per_seq = tiles;
       if (per_seq < 1) per_seq = 1;
       const int tpc = (int)((tiles + per_seq - 1) / per_seq);
       per_seq = (tiles + tpc - 1) / tpc;
-      dim3 grid((unsigned)per_seq, (unsigned)B);
-      k_index_scan_tma<<<grid, kTmaThreads, kTmaSmem, s>>>(map, qI, w, kI_seq_stride, rps, n, len_div, H_I, n_max, tpc,
-                                                           scores, scores_stride, hist, hdr, topk_k, st);
+      dim3 grid((unsigned)per_seq, (unsigned)units);
+#define CSA2_TMA_SCAN(R_)                                                                                  \
+  k_index_scan_tma<R_><<<grid, kTmaThreads, kTmaSmem, s>>>(map, qI, w, kI_seq_stride, rps, n, len_div, H_I, \
+                                                          n_max, tpc, scores, scores_stride, hist, hdr,     \
+                                                          topk_k, st)
+      if (R == 8) CSA2_TMA_SCAN(8);
+      else if (R == 4) CSA2_TMA_SCAN(4);
+      else if (R == 2) CSA2_TMA_SCAN(2);
+      else CSA2_TMA_SCAN(1);
+#undef CSA2_TMA_SCAN
       count_launch();
       return launch_status();
     }

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("R", [4, 2])
+@pytest.mark.parametrize("R", [4, 2, 8])
 def test_multi_token_decode_full_and_reindex_groups(R):
     S, W, H, L, P, k = 3, 128, 64, 2, 256, 512
     n_prev = [5000, 300, 90]                         # tokens cached before the step, per sequence
