@@ -53,12 +53,29 @@ int scan_init_attributes();
 int attn_tc_init_attributes();
 int launch_prefill_index(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys, float* scores,
                          int64_t stride, int32_t* st, cudaStream_t s);
-int attn_splits(int B, int H, int k, int W);
-size_t attn_ws_bytes(int B, int H, int k, int W);
-int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
-                       int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                       int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
-                       float softmax_scale, void* out, void* ws, int32_t* st, cudaStream_t s);
+size_t attn_ws_bytes(int64_t units, int H, int k, int W);
+size_t attn_group_ws_bytes(int64_t B, int H, int k, int W);
+int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                       int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
+                       int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, void* ws,
+                       int32_t* st, cudaStream_t s);
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// The layers [l0, l0 + L) of a group as one attention launch's operands.
+static bool attn_layers(AttnLayers* lay, const void* const* q, const void* const* swa, void* const* out, int l0,
+                        int L) {
+  *lay = AttnLayers{};
+  for (int i = 0; i < L; ++i) {
+    const void *qi = q[l0 + i], *si = swa[l0 + i];
+    void* oi = out[l0 + i];
+    if (!qi || !si || !oi || !aligned16(qi) || !aligned16(si) || !aligned16(oi)) return false;
+    lay->q[i] = static_cast<const __nv_bfloat16*>(qi);
+    lay->swa[i] = static_cast<const __nv_bfloat16*>(si);
+    lay->out[i] = static_cast<__nv_bfloat16*>(oi);
+  }
+  return true;
+}
 
 // ---- bookkeeping --------------------------------------------------------------
 static std::atomic<uint64_t> g_launches{0};
@@ -83,7 +100,6 @@ static int ensure_init() {
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 static bool ws_ok(const void* ws, size_t have, size_t need) {
   return need == 0 || (ws != nullptr && have >= need && (reinterpret_cast<uintptr_t>(ws) & 255) == 0);
 }
@@ -205,13 +221,13 @@ size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k, int3
     case CSA2_OP_PREFILL_GROUP: {
       // B = queries, n_max = entries: scores + Top-K + attention partials
       size_t m = align256((size_t)B * (size_t)n_max * 4) + topk_ws_bytes(B);
-      return m + attn_ws_bytes(B, H, k, 128);
+      return m + attn_group_ws_bytes(B, H, k, 128);
     }
     case CSA2_OP_FORM_POOL_BLOCK_MAX: return pool_block_max_ws_bytes(B, n_max);
     case CSA2_OP_LAYER_GROUP: {
       // the block-max pool reads the Full scores, so its workspace follows them
       size_t m = ws_index_full(B, n_max) + pool_block_max_ws_bytes(B, n_max);
-      const size_t r = ws_reindex(B, P), f = ws_form_pool(B, n_max), a = attn_ws_bytes(B, H, k, 128);
+      const size_t r = ws_reindex(B, P), f = ws_form_pool(B, n_max), a = attn_group_ws_bytes(B, H, k, 128);
       if (r > m) m = r;
       if (f > m) m = f;
       if (a > m) m = a;
@@ -416,9 +432,12 @@ int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d, const uint8
   if (!ws_ok(ws, ws_bytes, attn_ws_bytes(B, H, k, W))) return CSA2_ERR_WORKSPACE;
   int rc = ensure_init();
   if (rc != CSA2_OK) return rc;
-  return launch_sparse_attn(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
-                            swa_tail != 0, 1, swa_len, softmax_scale, out, ws, d_status,
-                            static_cast<cudaStream_t>(stream));
+  AttnLayers lay{};
+  lay.q[0] = static_cast<const __nv_bfloat16*>(q);
+  lay.swa[0] = static_cast<const __nv_bfloat16*>(swa);
+  lay.out[0] = static_cast<__nv_bfloat16*>(out);
+  return launch_sparse_attn(lay, 1, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa_seq_stride, W,
+                            swa_tail != 0, 1, swa_len, softmax_scale, ws, d_status, static_cast<cudaStream_t>(stream));
 }
 
 static cudaEvent_t group_event(const csa2_group_args* a, int i) {
@@ -475,15 +494,23 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
   }
   if (rc != CSA2_OK) return rc;
   if ((rc = rec(group_event(a, 2), s)) != CSA2_OK) return rc;
-  for (int l = 0; l <= a->n_reuse; ++l) {
-    if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
+  // the group's layers share the indices and the main KV: up to
+  // kMaxAttnLayers of them are attended by one launch (one CTA per row, layer
+  // and key split), so their set-up, tiles and epilogues overlap
+  const int n_layers = a->n_reuse + 1;
+  for (int l0 = 0; l0 < n_layers; l0 += kMaxAttnLayers) {
+    const int L = n_layers - l0 < kMaxAttnLayers ? n_layers - l0 : kMaxAttnLayers;
+    AttnLayers lay;
+    if (!attn_layers(&lay, a->q_layers, a->swa_layers, a->out_layers, l0, L)) return CSA2_ERR_INVALID_ARG;
     // one row per sequence: the layer's SWA ring (W rows, present keys first);
     // rps rows per sequence: W + rps - 1 linear rows, each window ending at its token
-    rc = launch_sparse_attn(a->q_layers[l], a->B, a->H, a->codes, a->scales, a->n_cap, a->n_cap, a->idx, a->k,
-                            a->swa_layers[l], rps > 1 ? a->W + rps - 1 : a->W, a->W, rps > 1 ? 1 : 0, rps,
-                            a->swa_len, a->softmax_scale, a->out_layers[l], a->ws, a->d_status, s);
+    rc = launch_sparse_attn(lay, L, a->B, a->H, a->codes, a->scales, a->n_cap, a->n_cap, a->idx, a->k,
+                            rps > 1 ? a->W + rps - 1 : a->W, a->W, rps > 1 ? 1 : 0, rps, a->swa_len,
+                            a->softmax_scale, a->ws, a->d_status, s);
     if (rc != CSA2_OK) return rc;
-    if ((rc = rec(group_event(a, 3 + l), s)) != CSA2_OK) return rc;
+    // event 3 + l marks the end of the launch that holds layer l
+    for (int l = l0; l < l0 + L; ++l)
+      if ((rc = rec(group_event(a, 3 + l), s)) != CSA2_OK) return rc;
   }
   return CSA2_OK;
 }
@@ -530,13 +557,16 @@ int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
   if ((rc = launch_topk(scores, nullptr, a->n_keys, a->n_vis, 1, a->Q, a->n_keys, a->k, a->idx, tk, false, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(ev(2), s)) != CSA2_OK) return rc;
-  for (int l = 0; l <= a->n_reuse; ++l) {
-    if (!a->q_layers[l] || !a->swa_layers[l] || !a->out_layers[l]) return CSA2_ERR_INVALID_ARG;
-    rc = launch_sparse_attn(a->q_layers[l], a->Q, a->H, a->codes, a->scales, 0, a->n_keys, a->idx, a->k,
-                            a->swa_layers[l], 1, a->W, 1, 1, a->swa_len, a->softmax_scale, a->out_layers[l], aws,
-                            a->d_status, s);
+  const int n_layers = a->n_reuse + 1;
+  for (int l0 = 0; l0 < n_layers; l0 += kMaxAttnLayers) {
+    const int L = n_layers - l0 < kMaxAttnLayers ? n_layers - l0 : kMaxAttnLayers;
+    AttnLayers lay;
+    if (!attn_layers(&lay, a->q_layers, a->swa_layers, a->out_layers, l0, L)) return CSA2_ERR_INVALID_ARG;
+    rc = launch_sparse_attn(lay, L, a->Q, a->H, a->codes, a->scales, 0, a->n_keys, a->idx, a->k, 1, a->W, 1, 1,
+                            a->swa_len, a->softmax_scale, aws, a->d_status, s);
     if (rc != CSA2_OK) return rc;
-    if ((rc = rec(ev(3 + l), s)) != CSA2_OK) return rc;
+    for (int l = l0; l < l0 + L; ++l)
+      if ((rc = rec(ev(3 + l), s)) != CSA2_OK) return rc;
   }
   return CSA2_OK;
 }

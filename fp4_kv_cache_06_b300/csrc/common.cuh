@@ -17,6 +17,16 @@
 namespace csa2 {
 
 constexpr int kSMs = 148;              // B300: 2 dies x 74 SMs
+constexpr int kMaxAttnLayers = 8;      // layers of one group attended by one launch
+
+// Per-layer operands of one attention launch (layer = blockIdx.z). The layers
+// share the Top-K indices and the FP4 main KV; each has its own queries
+// [B][H][512], SWA rows and output [B][H][512].
+struct AttnLayers {
+  const __nv_bfloat16* q[kMaxAttnLayers];
+  const __nv_bfloat16* swa[kMaxAttnLayers];
+  __nv_bfloat16* out[kMaxAttnLayers];
+};
 constexpr int kHistBins = 4096;        // level-0 Top-K histogram (12 key bits)
 constexpr int kCandCap = 8192;         // Top-K candidate buffer per row
 constexpr int kMaxTopK = 2048;

@@ -15,7 +15,8 @@ constexpr int kD = 512;          // main head dim
 constexpr int kTile = 64;        // keys per tile of the attention kernel
 
 // Log-sum-exp merge of split-K partials. Partial O is stored
-// [b][split][dim / 4][H][4] and (m, l) as [b][split][H][2]; one thread per
+// [layer][b][split][dim / 4][H][4] and (m, l) as [layer][b][split][H][2]
+// (layer = blockIdx.z, b = blockIdx.y); one thread per
 // (four dims, head) with heads fastest, so a warp's loads are contiguous. The
 // kernel is bound by load latency: U splits' loads are all issued before any
 // is used (U >= splits for decode shapes: one round trip), with an online
@@ -23,15 +24,17 @@ constexpr int kTile = 64;        // keys per tile of the attention kernel
 template <int U>
 __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ part_o,
                                                     const float* __restrict__ part_ml, int H, int splits,
-                                                    __nv_bfloat16* __restrict__ out) {
+                                                    const AttnLayers lay) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.y;
+  const int64_t unit = (int64_t)blockIdx.z * gridDim.y + b;
+  __nv_bfloat16* __restrict__ out = lay.out[blockIdx.z];
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (kD / 4) * H) return;
   const int d4 = i / H, h = i - d4 * H;
-  const float* ml = part_ml + ((int64_t)b * splits * H + h) * 2;
-  const float* po = part_o + ((int64_t)b * splits * (kD / 4) + d4) * H * 4 + h * 4;
+  const float* ml = part_ml + (unit * splits * H + h) * 2;
+  const float* po = part_o + (unit * splits * (kD / 4) + d4) * H * 4 + h * 4;
   const int64_t po_split = (int64_t)(kD / 4) * H * 4;
   float M = -INFINITY, Lsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -73,22 +76,23 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
 }
 
 // ---- host ------------------------------------------------------------------
-int launch_sparse_attn_tc(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
-                          int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                          int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
-                          float softmax_scale, void* out, float* part_o, float* part_ml, int splits, int tps,
-                          int32_t* st, cudaStream_t s);
+int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                          int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
+                          int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
+                          float* part_ml, int splits, int tps, int32_t* st, cudaStream_t s);
 
-// Split-K count. The attention kernel runs one CTA per SM (its shared memory
-// and all 512 TMEM columns). A batch that fills the machine runs unsplit (a
-// split writes an fp32 partial of H x 512 per CTA and needs the merge pass).
-// Otherwise minimise waves x tiles per split plus one tile-equivalent for
-// the merge; ties go to fewer splits.
-int attn_splits(int B, int H, int k, int W) {
+// Split-K count for `units` = rows x layers of one launch. The attention
+// kernel runs one CTA per SM (its shared memory and all 512 TMEM columns). A
+// launch that fills the machine runs unsplit (a split writes an fp32 partial
+// of H x 512 per CTA and needs the merge pass). Otherwise minimise
+// waves x tiles per split plus one tile-equivalent for the merge; ties go to
+// fewer splits.
+int attn_splits(int64_t units, int H, int k, int W) {
   (void)H;
   const int n_tiles = (k + W + kTile - 1) / kTile;
   const int64_t slots = kSMs;
-  if ((int64_t)B >= slots) return 1;
+  if (units >= slots) return 1;
+  const int64_t B = units;
   int best = 1;
   int64_t best_cost = -1;
   for (int s = 1; s <= n_tiles; ++s) {
@@ -102,38 +106,51 @@ int attn_splits(int B, int H, int k, int W) {
   return best;
 }
 
-size_t attn_ws_bytes(int B, int H, int k, int W) {
-  const int s = attn_splits(B, H, k, W);
+// Partials of one launch over `units` = rows x layers.
+size_t attn_ws_bytes(int64_t units, int H, int k, int W) {
+  const int s = attn_splits(units, H, k, W);
   if (s <= 1) return 0;
-  const size_t po = (size_t)B * s * H * kD * 4;
-  return ((po + 255) & ~(size_t)255) + (size_t)B * s * H * 2 * 4;
+  const size_t po = (size_t)units * s * H * kD * 4;
+  return ((po + 255) & ~(size_t)255) + (size_t)units * s * H * 2 * 4;
 }
 
-int launch_sparse_attn(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
-                       int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                       int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
-                       float softmax_scale, void* out, void* ws, int32_t* st, cudaStream_t s) {
-  if (B == 0) return CSA2_OK;
-  if (H < 1 || H > 64) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  const int splits = attn_splits(B, H, k, W);
+// Partials of a group of any size over B rows: the group is attended
+// kMaxAttnLayers layers per launch, so the largest launch has at most that many.
+size_t attn_group_ws_bytes(int64_t B, int H, int k, int W) {
+  size_t m = 0;
+  for (int L = 1; L <= kMaxAttnLayers; ++L) {
+    const size_t a = attn_ws_bytes(B * L, H, k, W);
+    if (a > m) m = a;
+  }
+  return m;
+}
+
+// Layers 0 .. L - 1 of `lay` (L <= kMaxAttnLayers) over rows 0 .. B - 1.
+int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                       int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
+                       int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, void* ws,
+                       int32_t* st, cudaStream_t s) {
+  if (B == 0 || L == 0) return CSA2_OK;
+  if (H < 1 || H > 64 || L < 0 || L > kMaxAttnLayers || B > 65535) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  const int64_t units = (int64_t)B * L;
+  const int splits = attn_splits(units, H, k, W);
   const int n_tiles = (k + W + kTile - 1) / kTile;
   const int tps = (n_tiles + splits - 1) / splits;
   float* part_o = nullptr;
   float* part_ml = nullptr;
   if (splits > 1) {
     part_o = static_cast<float*>(ws);
-    const size_t po = (size_t)B * splits * H * kD * 4;
+    const size_t po = (size_t)units * splits * H * kD * 4;
     part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + ((po + 255) & ~(size_t)255));
   }
-  int rc = launch_sparse_attn_tc(q, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa, swa_seq_stride, W,
-                                 swa_tail, rps < 1 ? 1 : rps, swa_len, softmax_scale, out, part_o, part_ml, splits,
-                                 tps, st, s);
+  int rc = launch_sparse_attn_tc(lay, L, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa_seq_stride, W,
+                                 swa_tail, rps < 1 ? 1 : rps, swa_len, softmax_scale, part_o, part_ml, splits, tps,
+                                 st, s);
   if (rc != CSA2_OK || splits == 1) return rc;
-  const dim3 grid((unsigned)(((kD / 4) * H + 127) / 128), (unsigned)B);
+  const dim3 grid((unsigned)(((kD / 4) * H + 127) / 128), (unsigned)B, (unsigned)L);
   auto kern = splits <= 4 ? k_attn_merge<4> : splits <= 8 ? k_attn_merge<8> : k_attn_merge<16>;
   const cudaError_t e = launch_pdl(kern, grid, dim3(128), 0, s, static_cast<const float*>(part_o),
-                                   static_cast<const float*>(part_ml), H, splits,
-                                   reinterpret_cast<__nv_bfloat16*>(out));
+                                   static_cast<const float*>(part_ml), H, splits, lay);
   count_launch();
   return launch_status(e);
 }

@@ -135,11 +135,10 @@ __device__ __forceinline__ uint32_t ldg_hint_u8(const void* p, uint64_t pol) {
 }
 
 __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
-    const __nv_bfloat16* __restrict__ q, int H, const uint8_t* __restrict__ codes,
-    const uint8_t* __restrict__ scales, int64_t kv_seq_stride, int64_t n_cap, const int32_t* __restrict__ idx,
-    int k, const __nv_bfloat16* __restrict__ swa, int64_t swa_seq_stride, int W, int swa_tail, int rps,
-    const int32_t* __restrict__ swa_len, float scale_log2, int splits, int tiles_per_split,
-    __nv_bfloat16* __restrict__ out, float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
+    const AttnLayers lay, int H, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+    int64_t kv_seq_stride, int64_t n_cap, const int32_t* __restrict__ idx, int k, int64_t swa_seq_stride, int W,
+    int swa_tail, int rps, const int32_t* __restrict__ swa_len, float scale_log2, int splits, int tiles_per_split,
+    float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;
@@ -153,7 +152,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   volatile uint32_t* sMisc = reinterpret_cast<volatile uint32_t*>(sp + L::kMisc);
   auto bar = [&](int i) { return base + L::kBar + 8u * (uint32_t)i; };
 
-  const int b = blockIdx.y, split = blockIdx.x;
+  const int b = blockIdx.y, split = blockIdx.x, layer = blockIdx.z;
+  const __nv_bfloat16* __restrict__ q = lay.q[layer];
+  const __nv_bfloat16* __restrict__ swa = lay.swa[layer];
+  __nv_bfloat16* __restrict__ out = lay.out[layer];
+  const int64_t unit = (int64_t)layer * gridDim.y + b;     // (layer, row) of the partials
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles = (k + W + kTT - 1) / kTT;
   const int t_begin = split * tiles_per_split;
@@ -525,7 +528,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         }
       } else {
         // partial O layout [b][split][dim / 4][H][4]: a warp stores 32 heads' float4 contiguously
-        float* o = part_o + ((((int64_t)b * splits + split) * (kTD / 4) + dim0 / 4) * H + h) * 4;
+        float* o = part_o + (((unit * splits + split) * (kTD / 4) + dim0 / 4) * H + h) * 4;
 #pragma unroll
         for (int x = 0; x < 64; x += 4)
           *reinterpret_cast<float4*>(o + (int64_t)(x / 4) * H * 4) =
@@ -534,7 +537,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       }
     }
     if (live && splits > 1 && row < 64 && chalf == 0) {
-      const int64_t pidx = ((int64_t)b * splits + split) * H + h;
+      const int64_t pidx = (unit * splits + split) * H + h;
       part_ml[pidx * 2 + 0] = sMx[h];
       part_ml[pidx * 2 + 1] = sL[h];
     }
@@ -554,17 +557,14 @@ int attn_tc_init_attributes() {
   return CSA2_OK;
 }
 
-int launch_sparse_attn_tc(const void* q, int B, int H, const uint8_t* codes, const uint8_t* scales,
-                          int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, const void* swa,
-                          int64_t swa_seq_stride, int W, int swa_tail, int rps, const int32_t* swa_len,
-                          float softmax_scale, void* out, float* part_o, float* part_ml, int splits, int tps,
-                          int32_t* st, cudaStream_t s) {
-  dim3 grid((unsigned)splits, (unsigned)B);
-  const cudaError_t e = launch_pdl(
-      k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, reinterpret_cast<const __nv_bfloat16*>(q), H,
-      codes, scales, kv_seq_stride, n_cap, idx, k, reinterpret_cast<const __nv_bfloat16*>(swa), swa_seq_stride, W,
-      swa_tail, rps, swa_len, softmax_scale * 1.4426950408889634f, splits, tps, reinterpret_cast<__nv_bfloat16*>(out),
-      part_o, part_ml, st);
+int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
+                          int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
+                          int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
+                          float* part_ml, int splits, int tps, int32_t* st, cudaStream_t s) {
+  dim3 grid((unsigned)splits, (unsigned)B, (unsigned)L);
+  const cudaError_t e = launch_pdl(k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, lay, H, codes, scales,
+                                   kv_seq_stride, n_cap, idx, k, swa_seq_stride, W, swa_tail, rps, swa_len,
+                                   softmax_scale * 1.4426950408889634f, splits, tps, part_o, part_ml, st);
   count_launch();
   return launch_status(e);
 }

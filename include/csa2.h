@@ -360,7 +360,9 @@ typedef struct csa2_group_args {
   void* const* events;   /* optional HOST array of cudaEvent_t recorded on
                             the stream: [0] the indexer scan begins, [1] the
                             scan ends, [2] Top-K (and pool) done, [3 + l]
-                            layer l's attention done                         */
+                            layer l's attention done. Up to 8 layers are
+                            attended by one launch, so the events of the
+                            layers in it are recorded together after it      */
   int32_t n_events;      /* length of `events` (0 = none)                     */
   int32_t rows_per_seq;  /* query rows per sequence, R (0 or 1: one). With
                             R > 1 (multi-token decode: R new tokens of each
@@ -425,7 +427,8 @@ typedef struct csa2_prefill_args {
   int32_t* d_status;     /* optional                                           */
   void* const* events;   /* optional HOST array of cudaEvent_t: [0] before the
                             indexer GEMM, [1] after it, [2] after Top-K,
-                            [3 + l] after layer l's attention                 */
+                            [3 + l] after layer l's attention (recorded
+                            together for the up to 8 layers of one launch)   */
   int32_t n_events;
 } csa2_prefill_args;
 

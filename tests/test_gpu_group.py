@@ -119,3 +119,21 @@ def test_reindex_group_with_pool_formation():
         ref_idx, ref_s, ref_pos = oracle.reindex_topk(u8(inp["qI"])[b], inp["w"].cpu().numpy()[b], u8(inp["kI"])[b], ref_pool, n)
         check_topk(gi[b], ref_idx, ref_s, ref_pos, 512)
         _check_layers(inp, outs, b, gi[b], ref_idx, c, s)
+
+
+@pytest.mark.parametrize("B", [2, 20])
+def test_group_of_eleven_layers(B):
+    """Full + 10 Reuse: the layers are attended in two launches (8 and 3
+    layers, so with different key splits at small batch); every layer equals
+    the oracle on the group's indices."""
+    n, H, L = 3000, 64, 11
+    inp = _group_inputs(B, n, n, H, 8, 128, L, seed=1100 + B)
+    idx, _, outs = _run(csa2.MODE_FULL, inp, n, L, P=512)
+    gi = idx.cpu().numpy()
+    for b in range(0, B, max(1, B // 4)):
+        c, s = oracle.quantize_fp4(bits16(inp["kv"])[b])
+        ref_idx, ref_s = oracle.full_topk(u8(inp["qI"])[b], inp["w"].cpu().numpy()[b], u8(inp["kI"])[b], n)
+        check_topk(gi[b], ref_idx, ref_s, np.arange(n), 512)
+        _check_layers(inp, outs, b, gi[b], ref_idx, c, s)
+    for l in range(1, L):
+        assert not torch.equal(outs[0], outs[l])
