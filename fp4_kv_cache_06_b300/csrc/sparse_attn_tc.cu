@@ -13,7 +13,7 @@
 // Key slots are processed in tiles of 64 (the layer's SWA rows first, so
 // their bf16 copies overlap the set-up and the first tile; then the gathered
 // rows) by a warp-specialised pipeline:
-//   producers (warps 4-11): row sources from the Top-K indices three tiles
+//   producers (warps 6-13): row sources from the Top-K indices three tiles
 //             ahead; the FP4 rows prefetched into registers two tiles ahead,
 //             then
 //             dequantised (E2M1 -> f16x2 hardware convert times the E4M3
@@ -24,15 +24,17 @@
 //             cp.async and converted in place (exact for magnitudes
 //             2^-14 .. 65504; smaller values keep 2^-24 absolute accuracy,
 //             larger ones saturate); absent rows are zero;
-//   MMA (warp 12, one thread): S(t) = Q K(t)^T with tcgen05.mma kind::f16,
+//   MMA (warp 14, one thread): S(t) = Q K(t)^T with tcgen05.mma kind::f16,
 //             M = 128 (heads padded from <= 64), N = 64 keys, K = 512, into one
 //             of two S buffers in TMEM, and O += P(t) V(t); each is issued as
 //             soon as its inputs are ready, so S(t+1) overlaps the softmax of
 //             tile t;
-//   softmax (warps 0-1, thread h = head h = TMEM lane h): reads S, raises the
-//             running max only when a tile exceeds it by more than 2^8
-//             (probabilities stay <= 256) and writes P (fp16); in the rare
-//             case of a raised max, warps 0-3 first rescale O in TMEM.
+//   softmax (warps 0, 1 for key columns 0..31 and 4, 5 for 32..63; thread =
+//             head = TMEM lane): reads S, takes the tile's per-head maximum
+//             across the two halves, raises the running max only when a
+//             tile exceeds it by more than 2^8 (probabilities stay <= 256)
+//             and writes P (fp16); in the rare case of a raised max, warps
+//             0-3 first rescale O in TMEM.
 // O for dims 0..255 accumulates in TMEM lanes 0..63 and dims 256..511 in
 // lanes 64..127 of the same 256 columns: two MMAs with A = [P; 0] and
 // A = [0; P] (zero rows leave the other half unchanged).
@@ -50,12 +52,14 @@ namespace csa2 {
 
 constexpr int kTD = 512;                  // head dim
 constexpr int kTT = 64;                   // keys per tile
-constexpr int kTThreads = 416;            // warps 0-3 softmax/correction, 4-11 producers, 12 MMA
-constexpr int kProdBase = 128;            // first producer thread
+constexpr int kTThreads = 480;            // warps 0-5 softmax/correction, 6-13 producers, 14 MMA
+constexpr int kSoftWarps = 6;
+constexpr int kSoftThreads = 32 * kSoftWarps;
+constexpr int kProdBase = kSoftThreads;   // first producer thread
 constexpr int kProd = 256;                // producer threads
 constexpr int kProdWarps = kProd / 32;
 constexpr int kItems = kTT / kProdWarps;  // FP4 rows per producer thread and tile (one 16-channel group each)
-constexpr int kMmaWarp = 12;
+constexpr int kMmaWarp = 14;
 constexpr int kRing = 8;                  // row-source ring: tiles j-2 .. j+3 may be live at once
 constexpr uint32_t kTOcol = 256;
 
@@ -69,7 +73,9 @@ struct TcSmem {                           // offsets from a 1024-aligned base
   static constexpr int kAlpha = kMask + kRing * 8;      // float[64]
   static constexpr int kL = kAlpha + 256;               // float[64]
   static constexpr int kM = kL + 256;                   // float[64]
-  static constexpr int kBar = kM + 256;                 // mbarriers (slots below)
+  static constexpr int kMaxPart = kM + 256;             // float[2][64]: per-head maxima of the two column halves
+  static constexpr int kLPart = kMaxPart + 512;         // float[64]: row sums of the upper column half
+  static constexpr int kBar = kLPart + 256;             // mbarriers (slots below)
   static constexpr int kMisc = kBar + 16 * 8;           // [0] tmem, [1..2] rescale flags, [3] abort
   static constexpr int kBytes = kMisc + 64 + 1024;      // + alignment slack
 };
@@ -147,6 +153,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   float* sAlpha = reinterpret_cast<float*>(sp + L::kAlpha);
   float* sL = reinterpret_cast<float*>(sp + L::kL);
   float* sMx = reinterpret_cast<float*>(sp + L::kM);
+  float* sMaxPart = reinterpret_cast<float*>(sp + L::kMaxPart);
+  float* sLPart = reinterpret_cast<float*>(sp + L::kLPart);
   int64_t* sSrc = reinterpret_cast<int64_t*>(sp + L::kSrc);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(sp + L::kMask);
   volatile uint32_t* sMisc = reinterpret_cast<volatile uint32_t*>(sp + L::kMisc);
@@ -245,9 +253,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   tc::fence_async_smem();
   __syncthreads();
 
-  float m_run = -INFINITY, l_run = 0.f;       // softmax threads (tid < 64): head tid
+  // softmax threads of warps 0, 1, 4, 5: head 32 (warp & 1) + lane; l_run
+  // sums the thread's column half, m_run is the same in both halves
+  float m_run = -INFINITY, l_run = 0.f;
 
-  if (warp >= 4 && warp < kMmaWarp) {
+  if (warp >= kSoftWarps && warp < kMmaWarp) {
     // ================= producers =================
     const int p = tid - kProdBase, pw = p >> 5, g = lane;
     // this thread's FP4 items of a tile: rows pw + kProdWarps i (i < kItems),
@@ -334,88 +344,100 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       if (j + 1 < nt && !produce(j + 1, cwB, sbB)) break;
     }
     cp_async_wait<0>();
-  } else if (warp < 4) {
+  } else if (warp < kSoftWarps) {
     // ================= softmax / O correction =================
+    // Warps 0, 1, 4 and 5 read S: TMEM lanes = heads 32 (warp & 1) + lane,
+    // key columns 32 (warp >> 2) .. + 31; the two halves exchange their
+    // per-head maxima through shared memory and keep their own row sums.
+    // Warps 0-3 rescale O (TMEM lanes 0-127) when a head raised its reference.
+    const bool reads_s = (warp & 3) < 2;
+    const int h = 32 * (warp & 1) + lane;
+    const int half = warp >> 2;
     for (int j = 0; j < nt; ++j) {
-      if (named_or(kNbSoft, 128, sMisc[3] != 0)) break;
+      if (named_or(kNbSoft, kSoftThreads, sMisc[3] != 0)) break;
       const int sbuf = j & 1;
-      if (warp < 2) {
-        bool ok = tc::mbar_wait(bar(kBarSFull + sbuf), (j >> 1) & 1);
+      uint32_t r[32];
+      bool ok = true;
+      if (reads_s) {
+        ok = tc::mbar_wait(bar(kBarSFull + sbuf), (j >> 1) & 1);
         ok = tc::mbar_wait(bar(kBarKvFull + sbuf), (j >> 1) & 1) && ok;     // orders the mask reads
         tc::tc_fence_after();
-        uint32_t r[64];
-        const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + 64u * sbuf;
-        tc::tmem_ld32(ta, r);
-        tc::tmem_ld32(ta + 32, r + 32);
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 1)) << 16) + 64u * sbuf + 32u * half, r);
         tc::tmem_ld_wait();
-        const int h = tid;
-        const uint32_t vm0 = sMask[(j % kRing) * 2], vm1 = sMask[(j % kRing) * 2 + 1];
-        float mt = -INFINITY;
+        const uint32_t vm = sMask[(j % kRing) * 2 + half];
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (vm != 0xffffffffu) {
 #pragma unroll
-        for (int x = 0; x < kTT; ++x) {
-          const bool valid = ((x < 32 ? vm0 : vm1) >> (x & 31)) & 1u;
-          const float v = valid ? __uint_as_float(r[x]) * scale_log2 : -INFINITY;
-          r[x] = __float_as_uint(v);
-          mt = fmaxf(mt, v);
+          for (int x = 0; x < 32; ++x)
+            if (!((vm >> x) & 1u)) r[x] = __float_as_uint(-INFINITY);
         }
+#pragma unroll
+        for (int x = 0; x < 32; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(r[x]));
+        sMaxPart[half * 64 + h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      }
+      named_sync(kNbSoft, kSoftThreads);
+      if (reads_s) {
+        // the scale is positive, so the scaled maximum is the maximum of the scaled scores
+        const float mt = fmaxf(sMaxPart[h], sMaxPart[64 + h]) * scale_log2;
         float alpha = 1.f;
         if (mt > m_run + 8.f) {               // raise the reference only when needed
           alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
           m_run = mt;
         }
-        const float base_m = (m_run == -INFINITY) ? 0.f : m_run;
+        const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
         // P and O are free once PV(j - 1) has finished
         if (j > 0) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1) && ok;
         if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
-        float sum = 0.f;
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
         unsigned char* prow = sp + L::kP + h * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
           uint32_t pk[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const __half2 pv = __floats2half2_rn(exp2f(__uint_as_float(r[8 * c + 2 * u]) - base_m),
-                                                 exp2f(__uint_as_float(r[8 * c + 2 * u + 1]) - base_m));
+            const __half2 pv = __floats2half2_rn(exp2f(fmaf(__uint_as_float(r[8 * c + 2 * u]), scale_log2, nbase)),
+                                                 exp2f(fmaf(__uint_as_float(r[8 * c + 2 * u + 1]), scale_log2, nbase)));
             const float2 f = __half22float2(pv);
-            sum += f.x + f.y;
+            sum[u] += f.x + f.y;
             pk[u] = *reinterpret_cast<const uint32_t*>(&pv);
           }
           const uint4 v4 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          const int sw = ((c ^ (h & 7)) << 4);
+          const int sw = (((4 * half + c) ^ (h & 7)) << 4);
           if (h < H) {
             *reinterpret_cast<uint4*>(prow + sw) = v4;               // P  (rows 0..63 of [P; Z])
             *reinterpret_cast<uint4*>(prow + 16384 + sw) = v4;       // P' (rows 64..127 of [Z; P'])
           }
         }
-        l_run = l_run * alpha + sum;
-        sAlpha[h] = alpha;
+        l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+        if (half == 0) sAlpha[h] = alpha;
         if (alpha != 1.f && j > 0) sMisc[1 + (j & 1)] = 1;
       }
-      named_sync(kNbSoft, 128);
+      named_sync(kNbSoft, kSoftThreads);
       // -- rescale O when some head raised its reference (rare)
-      if (sMisc[1 + (j & 1)]) {
+      if (sMisc[1 + (j & 1)] && warp < 4) {
         if (warp >= 2 && !tc::mbar_wait(bar(kBarODone), (j - 1) & 1)) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
         tc::tc_fence_after();
         const float a = sAlpha[(32 * warp + lane) & 63];
         const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + kTOcol;
         for (int c = 0; c < 256; c += 32) {
-          uint32_t r[32];
-          tc::tmem_ld32(ta + c, r);
+          uint32_t o[32];
+          tc::tmem_ld32(ta + c, o);
           tc::tmem_ld_wait();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * a);
-          tmem_st32(ta + c, r);
+          for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * a);
+          tmem_st32(ta + c, o);
         }
         tmem_st_wait();
       }
       tc::fence_async_smem();
       tc::tc_fence_before();
-      named_sync(kNbSoft, 128);
+      named_sync(kNbSoft, kSoftThreads);
       if (tid == 0) {
         sMisc[1 + (j & 1)] = 0;
         tc::mbar_arrive(bar(kBarPFull));
       }
     }
+    if (warp == 4 || warp == 5) sLPart[h] = l_run;
   } else {
     // ================= MMA issue (one thread) =================
     if (lane == 0) {
@@ -486,7 +508,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   tc::tc_fence_after();
   const bool have_o = nt > 0 && sMisc[3] == 0;  // uniform: read after the barrier
   if ((slen_in < 0 || slen_in > W) && split == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
-  if (tid < 64) { sL[tid] = have_o ? l_run : 0.f; sMx[tid] = have_o ? m_run : -INFINITY; }
+  if (tid < 64) { sL[tid] = have_o ? l_run + sLPart[tid] : 0.f; sMx[tid] = have_o ? m_run : -INFINITY; }
   __syncthreads();
   if (warp < 8) {
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (row r holds
