@@ -70,7 +70,8 @@ struct TcSmem {                           // offsets from a 1024-aligned base
   static constexpr int kP = kKV + 2 * kKVBytes;         // P | Z | P'  3 x 8 KB
   static constexpr int kSrc = kP + 3 * 8192;            // int64 [kRing][64]: >= 0 FP4 row, -1 absent, <= -2 SWA row
   static constexpr int kMask = kSrc + kRing * kTT * 8;  // u32 [kRing][2] valid keys
-  static constexpr int kAlpha = kMask + kRing * 8;      // float[64]
+  static constexpr int kFp4 = kMask + kRing * 8;        // u32 [kRing][2] keys that are FP4 rows
+  static constexpr int kAlpha = kFp4 + kRing * 8;       // float[64]
   static constexpr int kL = kAlpha + 256;               // float[64]
   static constexpr int kM = kL + 256;                   // float[64]
   static constexpr int kMaxPart = kM + 256;             // float[2][64]: per-head maxima of the two column halves
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   float* sLPart = reinterpret_cast<float*>(sp + L::kLPart);
   int64_t* sSrc = reinterpret_cast<int64_t*>(sp + L::kSrc);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(sp + L::kMask);
+  uint32_t* sFp4 = reinterpret_cast<uint32_t*>(sp + L::kFp4);
   volatile uint32_t* sMisc = reinterpret_cast<volatile uint32_t*>(sp + L::kMisc);
   auto bar = [&](int i) { return base + L::kBar + 8u * (uint32_t)i; };
 
@@ -225,7 +227,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     }
     sSrc[slot * kTT + p] = src;
     const uint32_t valid = __ballot_sync(0xffffffffu, src != -1);
-    if ((p & 31) == 0) sMask[slot * 2 + (p >> 5)] = valid;
+    const uint32_t fp4 = __ballot_sync(0xffffffffu, src >= 0);
+    if ((p & 31) == 0) {
+      sMask[slot * 2 + (p >> 5)] = valid;
+      sFp4[slot * 2 + (p >> 5)] = fp4;
+    }
   };
   if (tid < 64) {
     for (int j = 0; j < 3 && j < nt; ++j) row_sources(j, tid);
@@ -259,16 +265,20 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
 
   if (warp >= kSoftWarps && warp < kMmaWarp) {
     // ================= producers =================
-    const int p = tid - kProdBase, pw = p >> 5, g = lane;
-    // this thread's FP4 items of a tile: rows pw + kProdWarps i (i < kItems),
-    // 16-channel group g; two register sets hold tiles j and j + 1 in flight
+    const int p = tid - kProdBase, pw = p >> 5;
+    // this thread's FP4 items of a tile: rows 8 i + (lane & 7) (i < kItems),
+    // 16-channel group 4 pw + (lane >> 3). Per item a warp writes one 64-dim
+    // block of eight consecutive rows, so the eight lanes of a store
+    // wavefront hit eight distinct swizzle slots. Two register sets hold
+    // tiles j and j + 1 in flight.
+    const int rl = lane & 7, g = 4 * pw + (lane >> 3);
     uint2 cwA[kItems], cwB[kItems];
     uint32_t sbA[kItems], sbB[kItems];
     auto prefetch = [&](int j, uint2* cw, uint32_t* sb) {
       const int64_t* src = sSrc + (j % kRing) * kTT;
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
-        const int64_t s = src[pw + kProdWarps * i];
+        const int64_t s = src[8 * i + rl];
         cw[i] = make_uint2(0u, 0u);
         sb[i] = 0u;
         if (s >= 0) {
@@ -280,7 +290,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     // one tile: returns false when the group stops
     auto produce = [&](int j, uint2* cw, uint32_t* sb) -> bool {
       if (named_or(kNbProd, kProd, sMisc[3] != 0)) return false;
-      const int buf = j & 1;
+      const int buf = j & 1, slot = j % kRing;
       const uint32_t kv = base + L::kKV + buf * L::kKVBytes;
       unsigned char* kvp = sp + L::kKV + buf * L::kKVBytes;
       if (j + 3 < nt && p < 64) row_sources(j + 3, p);
@@ -289,26 +299,28 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         report(st, CSA2_ERR_TIMEOUT);
         sMisc[3] = 1;
       }
-      const int64_t* src = sSrc + (j % kRing) * kTT;
-      // SWA rows: bf16 straight into the key buffer (tile 0's came with Q); absent rows: zero
-      bool any_swa = false;
-      for (int e = p; e < kTT * 64; e += kProd) {
-        const int r = e >> 6, c = e & 63;
-        const int64_t s = src[r];
-        if (s >= 0) continue;
-        if (s == -1) {
-          *reinterpret_cast<uint4*>(kvp + kt_off(r, c)) = make_uint4(0, 0, 0, 0);
-        } else {
-          if (j > 0) cp_async16_hint(kv + kt_off(r, c), swa + (-2 - s) * kTD + c * 8, pol_stream);
-          any_swa = true;
+      const int64_t* src = sSrc + slot * kTT;
+      const uint64_t valid = (uint64_t)sMask[slot * 2] | ((uint64_t)sMask[slot * 2 + 1] << 32);
+      const uint64_t fp4 = (uint64_t)sFp4[slot * 2] | ((uint64_t)sFp4[slot * 2 + 1] << 32);
+      const uint64_t swa_rows = valid & ~fp4;
+      // absent rows: zero; SWA rows: bf16 straight into the key buffer (tile
+      // 0's came with Q). Warp pw takes rows pw + 8 m, a lane two 16-byte chunks.
+      if (~fp4 != 0) {
+        for (int r = pw; r < kTT; r += kProdWarps) {
+          if (!((valid >> r) & 1)) {
+            for (int c = lane; c < 64; c += 32) *reinterpret_cast<uint4*>(kvp + kt_off(r, c)) = make_uint4(0, 0, 0, 0);
+          } else if (j > 0 && ((swa_rows >> r) & 1)) {
+            const __nv_bfloat16* row = swa + (-2 - src[r]) * kTD;
+            for (int c = lane; c < 64; c += 32) cp_async16_hint(kv + kt_off(r, c), row + c * 8, pol_stream);
+          }
         }
       }
       cp_async_commit();
       // FP4 rows of this tile (in registers): one 16-channel group per item
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
-        const int r = pw + kProdWarps * i;
-        if (src[r] < 0) continue;
+        const int r = 8 * i + rl;
+        if (!((fp4 >> r) & 1)) continue;
         uint32_t sh2;                                           // scale as f16x2 {s, s}
         asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sh2) : "h"((uint16_t)(sb[i] | (sb[i] << 8))));
         uint32_t o[8];
@@ -321,20 +333,23 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         *reinterpret_cast<uint4*>(kvp + kt_off(r, 2 * g)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(kvp + kt_off(r, 2 * g + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      named_sync(kNbProd, kProd);             // row sources of j + 3 are in shared memory
-      if (j + 2 < nt) prefetch(j + 2, cw, sb);
-      if (named_or(kNbProd, kProd, any_swa)) {
+      // SWA rows: bf16 -> fp16 in place. Each thread converts the chunks it
+      // copied itself (tile 0's were copied and waited for during set-up).
+      if (swa_rows) {
         cp_async_wait<0>();
-        named_sync(kNbProd, kProd);
-        for (int e = p; e < kTT * 64; e += kProd) {          // SWA rows: bf16 -> fp16 in place
-          const int r = e >> 6, c = e & 63;
-          if (src[r] > -2) continue;
-          uint4* pv = reinterpret_cast<uint4*>(kvp + kt_off(r, c));
-          *pv = bf16x8_to_f16x8(*pv);
+        for (int r = pw; r < kTT; r += kProdWarps) {
+          if (!((swa_rows >> r) & 1)) continue;
+          for (int c = lane; c < 64; c += 32) {
+            uint4* pv = reinterpret_cast<uint4*>(kvp + kt_off(r, c));
+            *pv = bf16x8_to_f16x8(*pv);
+          }
         }
       }
       tc::fence_async_smem();
       tc::mbar_arrive(bar(kBarKvFull + buf));
+      // tile j + 2's row sources were written in produce(j - 1), before this
+      // call's opening barrier
+      if (j + 2 < nt) prefetch(j + 2, cw, sb);
       return true;
     };
     if (nt > 0) prefetch(0, cwA, sbA);
