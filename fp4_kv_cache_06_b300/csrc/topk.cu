@@ -369,80 +369,114 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
   }
 }
 
-// Digit d of a 1024-bin histogram (one bin per thread) at which the count
-// taken from the top reaches `need` (> 0, at most the histogram's sum):
-// *digit = d and *above = the count of entries in bins above d.
-__device__ void find_digit_from_top(const uint32_t* h, uint32_t need, uint32_t* s_warp, int* digit,
-                                    uint32_t* above) {
-  __shared__ int s_digit;
-  __shared__ uint32_t s_above;
-  const int d = kFinThreads - 1 - threadIdx.x;
-  const uint32_t c = h[d];
-  if (threadIdx.x == 0) { s_digit = 0; s_above = 0; }   // defined result even for an inconsistent histogram
-  uint32_t tot;
-  const uint32_t excl = block_excl_scan<kFinThreads>(c, s_warp, &tot);   // entries in bins above d
-  if (excl < need && excl + c >= need) { s_digit = d; s_above = excl; }
-  __syncthreads();
-  *digit = s_digit;
-  *above = s_above;
-  __syncthreads();
+// Digit d of a 1024-bin histogram at which the count taken from the top
+// reaches `need` (> 0, at most the histogram's sum), found by one warp: lane l
+// sums bins 1023 - 32 l - i (i < 32, read in a rotated order so the lanes hit
+// distinct banks), a warp scan picks the lane, and a second scan over that
+// lane's bins picks the digit. *digit = d and *above = the count in bins
+// above d (both 0 for an inconsistent histogram).
+__device__ void warp_digit_from_top(const uint32_t* h, uint32_t need, int* digit, uint32_t* above) {
+  const int lane = threadIdx.x & 31;
+  uint32_t sum = 0;
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) sum += h[1023 - 32 * lane - ((i + lane) & 31)];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += t;
+  }
+  const uint32_t excl = incl - sum;
+  const uint32_t hit = __ballot_sync(0xffffffffu, excl < need && incl >= need);
+  *digit = 0;
+  *above = 0;
+  if (!hit) return;
+  const int L = __ffs(hit) - 1;
+  const uint32_t base = __shfl_sync(0xffffffffu, excl, L);
+  const uint32_t c = h[1023 - 32 * L - lane];
+  uint32_t inc2 = c;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, inc2, off);
+    if (lane >= off) inc2 += t;
+  }
+  const uint32_t ex2 = base + inc2 - c;
+  const uint32_t hit2 = __ballot_sync(0xffffffffu, ex2 < need && ex2 + c >= need);
+  if (!hit2) return;
+  const int i = __ffs(hit2) - 1;
+  *digit = 1023 - 32 * L - i;
+  *above = __shfl_sync(0xffffffffu, ex2, i);
 }
 
 // Candidates keys[0..cnt) in index order with increasing positions, all at or
 // above threshold bin vbin: write the k best positions, ascending, to out.
+// h1, h2: two 1024-entry shared histograms; s_warp: the block scan's scratch.
 __device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, int32_t* __restrict__ out,
-                               uint32_t* h, uint32_t* s_warp) {
-  const int tid = threadIdx.x;
+                               uint32_t* h1, uint32_t* h2, uint32_t* s_warp) {
+  __shared__ uint32_t s_above, s_aA, s_aB;
+  __shared__ int s_dA, s_dB;
+  const int tid = threadIdx.x, lane = tid & 31;
   if (cnt <= k) {
     for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? cand_pos_of(keys[i]) : -1;
     return;
   }
-  // entries above the threshold bin are all taken
+  h1[tid] = 0;
+  h2[tid] = 0;
+  if (tid == 0) s_above = 0;
+  __syncthreads();
+  // entries above the threshold bin are all taken; score-key bits 19..10 of
+  // the entries in it
   uint32_t above = 0;
-  for (int i = tid; i < cnt; i += kFinThreads) above += (int)(keys[i] >> 52) > vbin;
-  uint32_t c_above;
-  block_excl_scan<kFinThreads>(above, s_warp, &c_above);
-  uint32_t need = (uint32_t)k - c_above;              // >= 1: the k-th score lies in the bin
-  // score-key bits 19..10 of the entries in the threshold bin
-  h[tid] = 0;
-  __syncthreads();
   for (int i = tid; i < cnt; i += kFinThreads) {
     const uint64_t key = keys[i];
-    if ((int)(key >> 52) == vbin) atomicAdd(&h[(key >> 42) & 1023], 1u);
+    const int bin = (int)(key >> 52);
+    if (bin > vbin) ++above;
+    else if (bin == vbin) atomicAdd(&h1[(key >> 42) & 1023], 1u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) above += __shfl_xor_sync(0xffffffffu, above, off);
+  if (lane == 0 && above) atomicAdd(&s_above, above);
+  __syncthreads();
+  if (tid < 32) {                                      // the k-th score lies in the bin: need >= 1
+    int d;
+    uint32_t a;
+    warp_digit_from_top(h1, (uint32_t)k - s_above, &d, &a);
+    if (lane == 0) { s_dA = d; s_aA = a; }
   }
   __syncthreads();
-  int dA, dB;
-  uint32_t aA, aB;
-  find_digit_from_top(h, need, s_warp, &dA, &aA);
-  need -= aA;
-  const uint64_t preA = ((uint64_t)vbin << 10) | (uint64_t)dA;   // score key >> 10
+  const uint32_t need = (uint32_t)k - s_above - s_aA;
+  const uint64_t preA = ((uint64_t)vbin << 10) | (uint64_t)s_dA;   // score key >> 10
   // score-key bits 9..0 of the entries sharing that prefix
-  h[tid] = 0;
-  __syncthreads();
   for (int i = tid; i < cnt; i += kFinThreads) {
     const uint64_t key = keys[i];
-    if ((key >> 42) == preA) atomicAdd(&h[(key >> 32) & 1023], 1u);
+    if ((key >> 42) == preA) atomicAdd(&h2[(key >> 32) & 1023], 1u);
   }
   __syncthreads();
-  find_digit_from_top(h, need, s_warp, &dB, &aB);
-  const uint32_t r = need - aB;                        // entries to take at exactly the k-th score
-  const uint32_t thr = (uint32_t)((preA << 10) | (uint64_t)dB);
-  // ordered output: thread t owns entries [lo, hi); ties at thr go to the
-  // first r in index order
+  if (tid < 32) {
+    int d;
+    uint32_t a;
+    warp_digit_from_top(h2, need, &d, &a);
+    if (lane == 0) { s_dB = d; s_aB = a; }
+  }
+  __syncthreads();
+  const uint32_t r = need - s_aB;                      // entries to take at exactly the k-th score
+  const uint32_t thr = (uint32_t)((preA << 10) | (uint64_t)s_dB);
+  // ordered output: thread t owns entries [lo, hi). One scan of the packed
+  // counts (strictly above | ties << 16; both < 2^16) gives both prefixes:
+  // the entry's slot is (above before it) + min(ties before it, r), as ties
+  // at thr go to the first r in index order.
   const int S = (cnt + kFinThreads - 1) / kFinThreads;
   const int lo = min(tid * S, cnt), hi = min(lo + S, cnt);
-  uint32_t ties = 0;
-  for (int i = lo; i < hi; ++i) ties += (uint32_t)(keys[i] >> 32) == thr;
-  uint32_t tot;
-  const uint32_t tie0 = block_excl_scan<kFinThreads>(ties, s_warp, &tot);
-  uint32_t takes = 0, tr = tie0;
+  uint32_t gt = 0, ties = 0;
   for (int i = lo; i < hi; ++i) {
     const uint32_t sk = (uint32_t)(keys[i] >> 32);
-    if (sk > thr) ++takes;
-    else if (sk == thr) takes += (tr++ < r) ? 1u : 0u;
+    gt += sk > thr;
+    ties += sk == thr;
   }
-  uint32_t o = block_excl_scan<kFinThreads>(takes, s_warp, &tot);   // tot == k
-  tr = tie0;
+  uint32_t tot;
+  const uint32_t pre = block_excl_scan<kFinThreads>(gt | (ties << 16), s_warp, &tot);
+  uint32_t tr = pre >> 16;
+  uint32_t o = (pre & 0xFFFFu) + min(tr, r);
   for (int i = lo; i < hi; ++i) {
     const uint32_t sk = (uint32_t)(keys[i] >> 32);
     bool take = sk > thr;
@@ -573,7 +607,7 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
       if (cand_pos_of(keys[i - 1]) >= cand_pos_of(keys[i])) mono = false;
   }
   if (__syncthreads_and(mono)) {
-    ordered_select(keys, cnt, vbin, k, out, h, s_warp);
+    ordered_select(keys, cnt, vbin, k, out, h, pre, s_warp);   // the chunk prefix is no longer needed
   } else {
     SmemKeys src{keys, cnt};
     select_and_write(src, k, cnt, out, h, sel);
