@@ -159,6 +159,85 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the workload
 # ---------------------------------------------------------------------------
+class PipelinedE2E:
+    """End-to-end steps as a server runs them: while step i computes, the
+    pinned host inputs of step i + 1 are copied in on one stream and the
+    outputs of step i are copied out on another. Two device sets of the
+    per-step inputs (the workload attributes named in `in_keys`) and of the
+    outputs alternate; events keep a set from being overwritten while a step
+    or a copy still uses it. Every step's input copy and output read-back runs
+    inside the caller's timed region: `begin` issues step 0's copy, step i
+    issues step i + 1's unless it is the last."""
+
+    def __init__(self, wl, in_keys):
+        torch = self.torch = wl.torch
+        self.wl, self.keys = wl, in_keys
+        clone = lambda v: [t.clone() for t in v] if isinstance(v, list) else v.clone()
+        self.sets = [{k: getattr(wl, k) for k in in_keys}, {k: clone(getattr(wl, k)) for k in in_keys}]
+        self.outs = [wl.out, [t.clone() for t in wl.out]]
+        self.h2d, self.d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+        self.in_ready, self.in_free, self.out_ready, self.out_free = ev(), ev(), ev(), ev()
+        self.used = [False, False]                       # set s has run a step (its free events are recorded)
+        self.i = 0
+
+    def _copy_in(self, s):
+        torch = self.torch
+        with torch.cuda.stream(self.h2d):
+            if self.used[s]:
+                self.h2d.wait_event(self.in_free[s])
+            for k in self.keys:
+                dst, src = self.sets[s][k], self.wl.h_in[k]
+                for d, h in (zip(dst, src) if isinstance(dst, list) else ((dst, src),)):
+                    d.copy_(h, non_blocking=True)
+            self.in_ready[s].record(self.h2d)
+
+    def begin(self):
+        """Start of a run of steps: step 0's inputs (after the caller's start
+        event). The caller has joined the previous run (`end`), so no set is
+        still in use."""
+        self.h2d.wait_stream(self.torch.cuda.current_stream())
+        self.d2h.wait_stream(self.torch.cuda.current_stream())
+        self.used = [False, False]
+        self.i = 0
+        self._copy_in(0)
+
+    def step(self, last):
+        torch, wl = self.torch, self.wl
+        s = self.i % 2
+        cur = torch.cuda.current_stream()
+        if not last:
+            self._copy_in(1 - s)
+        cur.wait_event(self.in_ready[s])
+        if self.used[s]:
+            cur.wait_event(self.out_free[s])             # step i - 2's outputs have been read back
+        for k in self.keys:
+            setattr(wl, k, self.sets[s][k])
+        wl.out = self.outs[s]
+        wl.step()
+        self.in_free[s].record(cur)
+        self.out_ready[s].record(cur)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.out_ready[s])
+            for h, d in zip(wl.h_out, self.outs[s]):
+                h.copy_(d, non_blocking=True)
+            self.out_free[s].record(self.d2h)
+        self.used[s] = True
+        self.i += 1
+
+    def end(self):
+        """Join the copy streams into the caller's stream (before its end event)."""
+        cur = self.torch.cuda.current_stream()
+        cur.wait_stream(self.d2h)
+        cur.wait_stream(self.h2d)
+
+    def restore(self):
+        """Bind the workload's original input and output tensors again."""
+        for k in self.keys:
+            setattr(self.wl, k, self.sets[0][k])
+        self.wl.out = self.outs[0]
+
+
 class DecodeWorkload:
     """Caches, per-layer inputs and the per-step calls of one decode config."""
 
@@ -291,21 +370,7 @@ class DecodeWorkload:
         d2h = sum(t.numel() * 2 for t in self.h_out)
         return h2d, d2h
 
-    def step_e2e(self):
-        hi = self.h_in
-        self.kv_new.copy_(hi["kv_new"], non_blocking=True)
-        self.kI_new.copy_(hi["kI_new"], non_blocking=True)
-        for d, s in zip(self.swa_new, hi["swa_new"]):
-            d.copy_(s, non_blocking=True)
-        for d, s in zip(self.q, hi["q"]):
-            d.copy_(s, non_blocking=True)
-        for d, s in zip(self.qI, hi["qI"]):
-            d.copy_(s, non_blocking=True)
-        for d, s in zip(self.w, hi["w"]):
-            d.copy_(s, non_blocking=True)
-        self.step()
-        for d, s in zip(self.h_out, self.out):
-            d.copy_(s, non_blocking=True)
+    E2E_INPUTS = ("kv_new", "kI_new", "swa_new", "q", "qI", "w")
 
 
 class MultiTokenWorkload(DecodeWorkload):
@@ -382,16 +447,7 @@ class MultiTokenWorkload(DecodeWorkload):
             sum(t.numel() * 2 for t in hi["q"]) + sum(t.numel() for t in hi["qI"]) + sum(t.numel() * 4 for t in hi["w"])
         return h2d, sum(t.numel() * 2 for t in self.h_out)
 
-    def step_e2e(self):
-        hi = self.h_in
-        self.kv_new.copy_(hi["kv_new"], non_blocking=True)
-        self.kI_new.copy_(hi["kI_new"], non_blocking=True)
-        for key, dst in (("swa", self.swa), ("q", self.q), ("qI", self.qI), ("w", self.w)):
-            for d, s in zip(dst, hi[key]):
-                d.copy_(s, non_blocking=True)
-        self.step()
-        for d, s in zip(self.h_out, self.out):
-            d.copy_(s, non_blocking=True)
+    E2E_INPUTS = ("kv_new", "kI_new", "swa", "q", "qI", "w")
 
 
 class EncoderDecodeWorkload(DecodeWorkload):
@@ -489,13 +545,7 @@ class EncoderDecodeWorkload(DecodeWorkload):
         h2d = sum(t.numel() * size[key] for key, ts in self.h_in.items() for t in ts)
         return h2d, sum(t.numel() * 2 for t in self.h_out)
 
-    def step_e2e(self):
-        for key in ("kv_new", "kI_new", "swa_new", "q", "qI", "w"):
-            for d, s in zip(getattr(self, key), self.h_in[key]):
-                d.copy_(s, non_blocking=True)
-        self.step()
-        for d, s in zip(self.h_out, self.out):
-            d.copy_(s, non_blocking=True)
+    E2E_INPUTS = ("kv_new", "kI_new", "swa_new", "q", "qI", "w")
 
 
 class PrefillWorkload:
@@ -776,27 +826,48 @@ def run_csa2(args, world, rank, local):
             "attn_ms_per_layer": statistics.mean(e[2 + j].elapsed_time(e[3 + j]) for e in ev for j in range(1 + nr)),
         }
 
-    # end-to-end: per-step inputs from pinned host memory, outputs back to host
+    # end-to-end: per-step inputs from pinned host memory, outputs back to host,
+    # the copies of neighbouring steps overlapping the compute (PipelinedE2E).
+    # Like the timed region, the K steps are one CUDA graph: every step's input
+    # copy, launches and read-back are nodes of it, replayed once.
     e2e = None
     if not args.no_e2e:
         h2d, d2h = wl.host_buffers()
+        pipe = PipelinedE2E(wl, wl.E2E_INPUTS)
         if cfg.steps > 1:
             wl.reset_positions()
-        for _ in range(2):
+        pipe.begin()
+        for i in range(2):
             maybe_wrap()
-            wl.step_e2e()
+            pipe.step(last=i == 1)
+        pipe.end()
+        torch.cuda.synchronize()
+        if cfg.steps > 1:
+            wl.reset_positions()
+            wl.step_i = 1                               # captured steps advance the positions
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph):
+            pipe.begin()
+            for i in range(args.steps):
+                pipe.step(last=i == args.steps - 1)
+            pipe.end()
+        if cfg.steps > 1:
+            wl.reset_positions()
+            wl.pos.sub_(1)                             # the first captured step adds 1
+            wl.n.sub_(1)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         e0.record()
-        for i in range(args.steps):
-            maybe_wrap()
-            wl.step_e2e()
+        e2e_graph.replay()
         e1.record()
+        pipe.restore()
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
         e2e = {"value": world * wl.tokens_per_step / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+               "schedule": "step i+1's inputs in and step i's outputs out on two copy streams during step i; "
+                           "K steps as one CUDA graph"}
 
     hbm, hbm_kind = peaks()
     roof = None
