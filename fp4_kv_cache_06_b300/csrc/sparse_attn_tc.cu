@@ -13,7 +13,7 @@
 // Key slots are processed in tiles of 64 (the layer's SWA rows first, so
 // their bf16 copies overlap the set-up and the first tile; then the gathered
 // rows) by a warp-specialised pipeline:
-//   producers (warps 6-13): row sources from the Top-K indices three tiles
+//   producers (warps 4-11): row sources from the Top-K indices three tiles
 //             ahead; the FP4 rows prefetched into registers two tiles ahead,
 //             then
 //             dequantised (E2M1 -> f16x2 hardware convert times the E4M3
@@ -24,21 +24,22 @@
 //             cp.async and converted in place (exact for magnitudes
 //             2^-14 .. 65504; smaller values keep 2^-24 absolute accuracy,
 //             larger ones saturate); absent rows are zero;
-//   MMA (warp 14, one thread): S(t) = Q K(t)^T with tcgen05.mma kind::f16,
-//             M = 128 (heads padded from <= 64), N = 64 keys, K = 512, into one
+//   MMA (warp 12, one thread): S(t) = Q K(t)^T with tcgen05.mma kind::f16,
+//             M = 64 heads, N = 64 keys, K = 512, into one
 //             of two S buffers in TMEM, and O += P(t) V(t); each is issued as
 //             soon as its inputs are ready, so S(t+1) overlaps the softmax of
 //             tile t;
-//   softmax (warps 0, 1 for key columns 0..31 and 4, 5 for 32..63; thread =
-//             head = TMEM lane): reads S, takes the tile's per-head maximum
-//             across the two halves, raises the running max only when a
+//   softmax (warps 0-3, two threads per head: key columns 0..31 and
+//             32..63): reads S, takes the tile's per-head maximum across the
+//             two halves by a shuffle, raises the running max only when a
 //             tile exceeds it by more than 2^8 (probabilities stay <= 256)
-//             and writes P (fp16); in the rare case of a raised max, warps
-//             0-3 first rescale O in TMEM.
+//             and writes P (fp16); in the rare case of a raised max, the same
+//             warps first rescale O in TMEM.
 // O for dims 0..255 accumulates in TMEM lanes 0..63 and dims 256..511 in
 // lanes 64..127 of the same 256 columns: two MMAs with A = [P; 0] and
 // A = [0; P] (zero rows leave the other half unchanged).
-// TMEM: S at columns 0..63 and 64..127, O at 256..511 (512 allocated, one CTA
+// TMEM: S at columns 0..63 and 64..127 (lanes 0-15 of each quadrant), O at
+// 256..511 (512 allocated, one CTA
 // per SM). Split-K partials (m, l, unnormalised O; O stored [dim/4][head][4]
 // so the epilogue's stores and the merge's loads are contiguous across heads)
 // are merged by the log-sum-exp merge kernel. Every wait is bounded; after a
@@ -52,14 +53,14 @@ namespace csa2 {
 
 constexpr int kTD = 512;                  // head dim
 constexpr int kTT = 64;                   // keys per tile
-constexpr int kTThreads = 480;            // warps 0-5 softmax/correction, 6-13 producers, 14 MMA
-constexpr int kSoftWarps = 6;
+constexpr int kTThreads = 416;            // warps 0-3 softmax/correction, 4-11 producers, 12 MMA
+constexpr int kSoftWarps = 4;
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kProdBase = kSoftThreads;   // first producer thread
 constexpr int kProd = 256;                // producer threads
 constexpr int kProdWarps = kProd / 32;
 constexpr int kItems = kTT / kProdWarps;  // FP4 rows per producer thread and tile (one 16-channel group each)
-constexpr int kMmaWarp = 14;
+constexpr int kMmaWarp = 12;
 constexpr int kRing = 8;                  // row-source ring: tiles j-2 .. j+3 may be live at once
 constexpr uint32_t kTOcol = 256;
 
@@ -74,9 +75,7 @@ struct TcSmem {                           // offsets from a 1024-aligned base
   static constexpr int kAlpha = kFp4 + kRing * 8;       // float[64]
   static constexpr int kL = kAlpha + 256;               // float[64]
   static constexpr int kM = kL + 256;                   // float[64]
-  static constexpr int kMaxPart = kM + 256;             // float[2][64]: per-head maxima of the two column halves
-  static constexpr int kLPart = kMaxPart + 512;         // float[64]: row sums of the upper column half
-  static constexpr int kBar = kLPart + 256;             // mbarriers (slots below)
+  static constexpr int kBar = kM + 256;                 // mbarriers (slots below)
   static constexpr int kMisc = kBar + 16 * 8;           // [0] tmem, [1..2] rescale flags, [3] abort
   static constexpr int kBytes = kMisc + 64 + 1024;      // + alignment slack
 };
@@ -112,6 +111,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
         "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
         "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
+}
+// 16x32bx2.x32: lanes 0-15 of the warp's TMEM quadrant; thread t < 16 gets
+// lane t, columns c..c+31, thread t >= 16 gets lane t - 16, columns c+32..c+63
+__device__ __forceinline__ void tmem_ld_16x32bx2_32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -154,8 +165,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   float* sAlpha = reinterpret_cast<float*>(sp + L::kAlpha);
   float* sL = reinterpret_cast<float*>(sp + L::kL);
   float* sMx = reinterpret_cast<float*>(sp + L::kM);
-  float* sMaxPart = reinterpret_cast<float*>(sp + L::kMaxPart);
-  float* sLPart = reinterpret_cast<float*>(sp + L::kLPart);
   int64_t* sSrc = reinterpret_cast<int64_t*>(sp + L::kSrc);
   uint32_t* sMask = reinterpret_cast<uint32_t*>(sp + L::kMask);
   uint32_t* sFp4 = reinterpret_cast<uint32_t*>(sp + L::kFp4);
@@ -259,9 +268,10 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   tc::fence_async_smem();
   __syncthreads();
 
-  // softmax threads of warps 0, 1, 4, 5: head 32 (warp & 1) + lane; l_run
-  // sums the thread's column half, m_run is the same in both halves
-  float m_run = -INFINITY, l_run = 0.f;
+  // softmax threads (warps 0-3): head 16 warp + (lane & 15), key columns
+  // 32 (lane >> 4) .. + 31 of a tile; l_run sums the thread's column half,
+  // m_run is the same in both halves, l_tot is the head's total
+  float m_run = -INFINITY, l_run = 0.f, l_tot = 0.f;
 
   if (warp >= kSoftWarps && warp < kMmaWarp) {
     // ================= producers =================
@@ -361,76 +371,71 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     cp_async_wait<0>();
   } else if (warp < kSoftWarps) {
     // ================= softmax / O correction =================
-    // Warps 0, 1, 4 and 5 read S: TMEM lanes = heads 32 (warp & 1) + lane,
-    // key columns 32 (warp >> 2) .. + 31; the two halves exchange their
-    // per-head maxima through shared memory and keep their own row sums.
-    // Warps 0-3 rescale O (TMEM lanes 0-127) when a head raised its reference.
-    const bool reads_s = (warp & 3) < 2;
-    const int h = 32 * (warp & 1) + lane;
-    const int half = warp >> 2;
+    // S(t) is an M = 64 accumulator: head h in TMEM lane 32 (h / 16) + h % 16.
+    // Warp q reads heads 16 q .. + 15 with the 16x32bx2 shape: lanes 0-15 get
+    // key columns 0..31, lanes 16-31 columns 32..63 of the same heads, so the
+    // two halves of a head exchange their maxima and sums by one shuffle.
+    // Warps 0-3 also rescale O (TMEM lanes 0-127) when a head raised its
+    // reference.
+    const int h = 16 * warp + (lane & 15);
+    const int half = lane >> 4;
     for (int j = 0; j < nt; ++j) {
       if (named_or(kNbSoft, kSoftThreads, sMisc[3] != 0)) break;
       const int sbuf = j & 1;
       uint32_t r[32];
-      bool ok = true;
-      if (reads_s) {
-        ok = tc::mbar_wait(bar(kBarSFull + sbuf), (j >> 1) & 1);
-        ok = tc::mbar_wait(bar(kBarKvFull + sbuf), (j >> 1) & 1) && ok;     // orders the mask reads
-        tc::tc_fence_after();
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * (warp & 1)) << 16) + 64u * sbuf + 32u * half, r);
-        tc::tmem_ld_wait();
-        const uint32_t vm = sMask[(j % kRing) * 2 + half];
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (vm != 0xffffffffu) {
+      bool ok = tc::mbar_wait(bar(kBarSFull + sbuf), (j >> 1) & 1);
+      ok = tc::mbar_wait(bar(kBarKvFull + sbuf), (j >> 1) & 1) && ok;     // orders the mask reads
+      tc::tc_fence_after();
+      tmem_ld_16x32bx2_32(tmem + ((uint32_t)(32 * warp) << 16) + 64u * sbuf, r);
+      tc::tmem_ld_wait();
+      const uint32_t vm = sMask[(j % kRing) * 2 + half];
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (vm != 0xffffffffu) {
 #pragma unroll
-          for (int x = 0; x < 32; ++x)
-            if (!((vm >> x) & 1u)) r[x] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int x = 0; x < 32; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(r[x]));
-        sMaxPart[half * 64 + h] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        for (int x = 0; x < 32; ++x)
+          if (!((vm >> x) & 1u)) r[x] = __float_as_uint(-INFINITY);
       }
-      named_sync(kNbSoft, kSoftThreads);
-      if (reads_s) {
-        // the scale is positive, so the scaled maximum is the maximum of the scaled scores
-        const float mt = fmaxf(sMaxPart[h], sMaxPart[64 + h]) * scale_log2;
-        float alpha = 1.f;
-        if (mt > m_run + 8.f) {               // raise the reference only when needed
-          alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
-          m_run = mt;
-        }
-        const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
-        // P and O are free once PV(j - 1) has finished
-        if (j > 0) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1) && ok;
-        if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
-        float sum[4] = {0.f, 0.f, 0.f, 0.f};
-        unsigned char* prow = sp + L::kP + h * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const __half2 pv = __floats2half2_rn(exp2f(fmaf(__uint_as_float(r[8 * c + 2 * u]), scale_log2, nbase)),
-                                                 exp2f(fmaf(__uint_as_float(r[8 * c + 2 * u + 1]), scale_log2, nbase)));
-            const float2 f = __half22float2(pv);
-            sum[u] += f.x + f.y;
-            pk[u] = *reinterpret_cast<const uint32_t*>(&pv);
-          }
-          const uint4 v4 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          const int sw = (((4 * half + c) ^ (h & 7)) << 4);
-          if (h < H) {
-            *reinterpret_cast<uint4*>(prow + sw) = v4;               // P  (rows 0..63 of [P; Z])
-            *reinterpret_cast<uint4*>(prow + 16384 + sw) = v4;       // P' (rows 64..127 of [Z; P'])
-          }
-        }
-        l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
-        if (half == 0) sAlpha[h] = alpha;
-        if (alpha != 1.f && j > 0) sMisc[1 + (j & 1)] = 1;
+      for (int x = 0; x < 32; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(r[x]));
+      float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
+      // the scale is positive, so the scaled maximum is the maximum of the scaled scores
+      const float mt = mh * scale_log2;
+      float alpha = 1.f;
+      if (mt > m_run + 8.f) {                 // raise the reference only when needed
+        alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
+        m_run = mt;
       }
+      const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
+      // P and O are free once PV(j - 1) has finished
+      if (j > 0) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1) && ok;
+      if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      unsigned char* prow = sp + L::kP + h * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const __half2 pv = __floats2half2_rn(exp2f(fmaf(__uint_as_float(r[8 * c + 2 * u]), scale_log2, nbase)),
+                                               exp2f(fmaf(__uint_as_float(r[8 * c + 2 * u + 1]), scale_log2, nbase)));
+          const float2 f = __half22float2(pv);
+          sum[u] += f.x + f.y;
+          pk[u] = *reinterpret_cast<const uint32_t*>(&pv);
+        }
+        const uint4 v4 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        const int sw = (((4 * half + c) ^ (h & 7)) << 4);
+        if (h < H) {
+          *reinterpret_cast<uint4*>(prow + sw) = v4;               // P  (rows 0..63 of [P; Z])
+          *reinterpret_cast<uint4*>(prow + 16384 + sw) = v4;       // P' (rows 64..127 of [Z; P'])
+        }
+      }
+      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      if (half == 0) sAlpha[h] = alpha;
+      if (alpha != 1.f && j > 0) sMisc[1 + (j & 1)] = 1;
       named_sync(kNbSoft, kSoftThreads);
       // -- rescale O when some head raised its reference (rare)
-      if (sMisc[1 + (j & 1)] && warp < 4) {
-        if (warp >= 2 && !tc::mbar_wait(bar(kBarODone), (j - 1) & 1)) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
+      if (sMisc[1 + (j & 1)]) {
         tc::tc_fence_after();
         const float a = sAlpha[(32 * warp + lane) & 63];
         const uint32_t ta = tmem + ((uint32_t)(32 * warp) << 16) + kTOcol;
@@ -452,11 +457,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         tc::mbar_arrive(bar(kBarPFull));
       }
     }
-    if (warp == 4 || warp == 5) sLPart[h] = l_run;
+    l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
   } else {
     // ================= MMA issue (one thread) =================
     if (lane == 0) {
-      const uint32_t idesc_s = tc::instr_desc(tc::kFmtF16, tc::kFmtF16, 0, 0, 128, kTT);
+      const uint32_t idesc_s = tc::instr_desc(tc::kFmtF16, tc::kFmtF16, 0, 0, 64, kTT);   // heads: M = 64
       const uint32_t idesc_o = tc::instr_desc(tc::kFmtF16, tc::kFmtF16, 0, 1, 128, 256);
       auto issue_pv = [&](int j) {
         const uint32_t kv = base + L::kKV + (j & 1) * L::kKVBytes;
@@ -523,7 +528,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   tc::tc_fence_after();
   const bool have_o = nt > 0 && sMisc[3] == 0;  // uniform: read after the barrier
   if ((slen_in < 0 || slen_in > W) && split == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
-  if (tid < 64) { sL[tid] = have_o ? l_run + sLPart[tid] : 0.f; sMx[tid] = have_o ? m_run : -INFINITY; }
+  if (warp < kSoftWarps && lane < 16) {
+    const int h = 16 * warp + lane;
+    sL[h] = have_o ? l_tot : 0.f;
+    sMx[h] = have_o ? m_run : -INFINITY;
+  }
   __syncthreads();
   if (warp < 8) {
     // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (row r holds
