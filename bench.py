@@ -631,14 +631,21 @@ def run_prefill(args, world, rank, local):
     evs = [[[mk() for _ in range(3 + L)] for L in wl.group_layers] for _ in range(args.steps)]
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
     torch.cuda.synchronize()
+    # the timed graph has only the step events (an event between two launches
+    # would cancel their programmatic overlap); the phase graph, replayed after
+    # it, has the per-group events
     launches0 = csa2.launch_count()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for i in range(args.steps):
             step_ev[i][0].record()
-            wl.step(events=evs[i])
+            wl.step()
             step_ev[i][1].record()
     launches = csa2.launch_count() - launches0
+    pgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pgraph):
+        for i in range(args.steps):
+            wl.step(events=evs[i])
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
@@ -651,6 +658,8 @@ def run_prefill(args, world, rank, local):
     barrier(world)
     ms = statistics.mean(a.elapsed_time(b) for a, b in step_ev)
     ms_max = max_over_ranks(ms, world, dev)
+    pgraph.replay()
+    torch.cuda.synchronize()
     gemm_ms = statistics.mean(e[0].elapsed_time(e[1]) for es in evs for e in es)
     topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for es in evs for e in es)
     attn_ms = statistics.mean(e[2 + j].elapsed_time(e[3 + j]) for es in evs for g, e in enumerate(es)
@@ -781,22 +790,35 @@ def run_csa2(args, world, rank, local):
     step_ev = [(mk(), mk()) for _ in range(args.steps)]
     grp_ev = [[[mk() for _ in range(3 + 1 + cfg.groups[g][1])] for g in range(G)] for _ in range(args.steps)]
     torch.cuda.synchronize()
-    if cfg.steps > 1:
-        wl.reset_positions()
-        wl.step_i = 1                                   # captured steps advance the positions
+
+    def capture(phases):
+        """K steps as one graph: the timed one has only the step events (an
+        event between two launches would cancel their programmatic overlap);
+        the phase one (replayed separately) has the per-group events."""
+        if cfg.steps > 1:
+            wl.reset_positions()
+            wl.step_i = 1                               # captured steps advance the positions
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(args.steps):
+                flush()                                # evict L2 between steps (outside the step events)
+                if not phases:
+                    step_ev[i][0].record()
+                wl.step(events=grp_ev[i] if phases else None)
+                if not phases:
+                    step_ev[i][1].record()
+        return g
+
+    def rewind():
+        if cfg.steps > 1:
+            wl.reset_positions()
+            wl.pos.sub_(1)                             # the first captured step adds 1
+            wl.n.sub_(1)
+
     launches0 = csa2.launch_count()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(args.steps):
-            flush()                                    # evict L2 between steps (outside the step events)
-            step_ev[i][0].record()
-            wl.step(events=grp_ev[i])
-            step_ev[i][1].record()
+    graph = capture(False)
     launches = csa2.launch_count() - launches0        # kernels launched per replay of the timed graph
-    if cfg.steps > 1:
-        wl.reset_positions()
-        wl.pos.sub_(1)                                 # the first captured step adds 1
-        wl.n.sub_(1)
+    rewind()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -811,6 +833,13 @@ def run_csa2(args, world, rank, local):
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     ms = statistics.mean(step_ms)
     ms_max = max_over_ranks(ms, world, dev)
+    # the phase breakdown (and the scan's duration for the roofline) from a
+    # second replay with the per-group events
+    pgraph = capture(True)
+    rewind()
+    torch.cuda.synchronize()
+    pgraph.replay()
+    torch.cuda.synchronize()
     # Full scan duration (events 0 -> 1 of each Full group)
     scan_ms = []
     for i in range(args.steps):
