@@ -207,3 +207,46 @@ def test_full_group_block_max_pool_holds_every_top_position():
         ref_pool, ref_bs = oracle.form_pool_block_max(ref_s, n, P)
         check_topk(gp[b], ref_pool, ref_bs, np.arange(ref_bs.size), P)
         assert set((gi[b] // 8).tolist()) <= set(gp[b].tolist())
+
+
+@pytest.mark.parametrize("k", [512, 2048])
+def test_topk_many_long_rows(k):
+    """Many position rows longer than 32K entries (ordered compaction, chunk
+    table, ordered select): rows with heavy exact ties, an all-tied row (more
+    than 8192 candidates in the threshold bin: the slow path), ragged and empty
+    rows; every row exact."""
+    rng = np.random.default_rng(k)
+    B, m = 20, 70000
+    s = rng.standard_normal((B, m)).astype(np.float32)
+    s[1] = rng.integers(0, 50, m)
+    s[2] = 0.0
+    s[3] = rng.integers(0, 3, m)
+    n_list = [m] * B
+    n_list[4], n_list[5], n_list[6], n_list[7] = 100, 0, 511, 33000
+    n = torch.tensor(n_list, dtype=torch.int64, device=DEV)
+    idx = torch.empty((B, k), dtype=torch.int32, device=DEV)
+    ws = _ws(csa2.OP_TOPK, B, m, k)
+    csa2.csa2_topk(torch.from_numpy(s).to(DEV), n, m, k, idx, ws)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    for b in range(B):
+        ref = oracle.topk_select(s[b, :n_list[b]].astype(np.float64), np.arange(n_list[b]), k)
+        np.testing.assert_array_equal(gi[b], ref)
+
+
+@pytest.mark.parametrize("k", [512, 2048])
+def test_index_full_many_long_rows_topk(k):
+    """The Full scan's fused histogram feeding Top-K on many rows past the
+    short-row limit."""
+    B, n_cap = 17, 40000
+    n_list = [40000] * 16 + [35001]
+    kI, qI, w = _inputs(B, n_cap, 8, 128, seed=33, bias=0.05)
+    n = torch.tensor(n_list, dtype=torch.int64, device=DEV)
+    idx = torch.empty((B, k), dtype=torch.int32, device=DEV)
+    ws = _ws(csa2.OP_INDEX_FULL, B, n_cap, k)
+    csa2.csa2_index_full(qI.to(DEV), w.to(DEV), kI.to(DEV), n, n_cap, k, idx, ws)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    for b in range(0, B, 4):
+        ref_idx, ref_s = oracle.full_topk(u8(qI)[b], w.numpy()[b], u8(kI)[b], n_list[b], k)
+        check_topk(gi[b], ref_idx, ref_s, np.arange(n_list[b]), k)
