@@ -22,6 +22,7 @@ OP_PREFILL_GROUP = 7
 OP_FORM_POOL_BLOCK_MAX = 8
 POOL_NONE, POOL_MEAN_KEY, POOL_BLOCK_MAX = 0, 1, 2
 MODE_FULL, MODE_REINDEX = 0, 1
+TOPK_NOALLOC_MAX_ROWS = 64          # CSA2_TOPK_NOALLOC_MAX_ROWS
 
 EXPORTS = (
     "csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size",

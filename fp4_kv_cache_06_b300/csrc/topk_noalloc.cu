@@ -13,7 +13,8 @@
 // until the process exits. Nothing is allocated per call.
 //
 // The array holds the scratch of csa2_topk for at most
-// CSA2_TOPK_NOALLOC_MAX_ROWS rows (about 7.25 MB). All calls share it and it
+// CSA2_TOPK_NOALLOC_MAX_ROWS rows: 7,341,056 bytes (7.0 MiB), exactly the
+// workspace csa2_topk needs for that many rows. All calls share it and it
 // keeps whatever the last call left there; each call clears the part that
 // must start at zero (the histograms and row headers) before use. Calls that
 // overlap on the GPU — on two streams, or from two host threads without

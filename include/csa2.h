@@ -226,7 +226,8 @@ CSA2_API int csa2_topk(const float* scores, const int32_t* cand_pos,
  * Same selection, arguments and result as csa2_topk, minus the workspace:
  * the scratch lives in a fixed device array inside the library, reserved on
  * every GPU that loads the library and held until the process exits
- * (about 7.25 MB). Limits: at most CSA2_TOPK_NOALLOC_MAX_ROWS rows (B);
+ * (7,341,056 bytes = 7.0 MiB, the csa2_topk workspace of
+ * CSA2_TOPK_NOALLOC_MAX_ROWS rows). Limits: at most CSA2_TOPK_NOALLOC_MAX_ROWS rows (B);
  * larger B returns CSA2_ERR_UNSUPPORTED_SHAPE and enqueues nothing.
  * The first call made while a device is current looks up that device's
  * array address (one-time set-up); make that first call before capturing

@@ -1,4 +1,4 @@
-"""csa2_topk_noalloc against csa2_topk, through the C ABI.
+"""csa2_topk_noalloc against csa2_topk and the oracle, through the C ABI.
 
 The no-workspace entry point exists for callers that cannot allocate
 device memory (plugin hooks where allocation is forbidden, allocation-free
@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from fp4_kv_cache_06_b300 import csa2
 
 pytestmark = pytest.mark.gpu
@@ -51,9 +52,59 @@ def test_noalloc_matches_workspace_version_on_two_calls():
     torch.cuda.synchronize()
     assert torch.equal(a1, b1)
     assert torch.equal(a2, b2)
+    for b, ref in _oracle_rows(s1, n1, 512, [0, 1, 17, 39]).items():
+        np.testing.assert_array_equal(a1[b].cpu().numpy(), ref)
+    for b, ref in _oracle_rows(s2, None, 2048, [0, 6], cand_pos=cp).items():
+        np.testing.assert_array_equal(a2[b].cpu().numpy(), ref)
     # sanity: the selection is a sorted, -1 padded index list
     r = a1.cpu().numpy()[1]
     assert np.all(r[:100] == np.arange(100)) and np.all(r[100:] == -1)
+
+
+def _oracle_rows(scores, n, k, rows, cand_pos=None):
+    """The oracle's selection for a few rows (fp32 scores are exact in float64)."""
+    s = scores.cpu().double().numpy()
+    n_h = None if n is None else n.cpu().numpy()
+    cp = None if cand_pos is None else cand_pos.cpu().numpy()
+    out = {}
+    for b in rows:
+        m = s.shape[1] if n_h is None else int(n_h[b])
+        pos = np.arange(m) if cp is None else cp[b, :m]
+        out[b] = oracle.topk_select(s[b, :m], pos, k)
+    return out
+
+
+def test_noalloc_full_scratch_after_other_shapes():
+    """Two more calls after differently shaped ones, at the row limit where the
+    scratch is exactly full: long ragged rows (the chunk-table path, whose
+    tables now start at offsets set by the new row count) and caller-given
+    candidate positions with absent entries. Each is compared with csa2_topk
+    and, on sampled rows, with the oracle."""
+    g = torch.Generator(device="cpu").manual_seed(11)
+    B, n_max, k = csa2.TOPK_NOALLOC_MAX_ROWS, 40000, 512
+    # small call first, so the scratch holds another shape's leftovers
+    s0 = torch.rand((3, 5000), generator=g).to(DEV)
+    _without_workspace(s0, None, 5000, 64)
+    s3 = torch.randint(0, 3000, (B, n_max), generator=g).to(torch.float32).to(DEV) / 7.0
+    n3 = torch.randint(20000, n_max + 1, (B,), generator=g).to(torch.int64)
+    n3[5] = 300                                        # fewer than k candidates
+    n3[9] = n_max
+    n3 = n3.to(DEV)
+    a3 = _without_workspace(s3, n3, n_max, k)
+    b3 = _with_workspace(s3, n3, n_max, k)
+    cp = torch.randperm(10 ** 7, generator=g)[:B * n_max].reshape(B, n_max).to(torch.int32)
+    cp[torch.rand((B, n_max), generator=g) < 0.3] = -1
+    cp = cp.to(DEV)
+    a4 = _without_workspace(s3, n3, n_max, k, cand_pos=cp)
+    b4 = _with_workspace(s3, n3, n_max, k, cand_pos=cp)
+    torch.cuda.synchronize()
+    assert torch.equal(a3, b3)
+    assert torch.equal(a4, b4)
+    rows = [0, 5, 9, 33, B - 1]
+    for b, ref in _oracle_rows(s3, n3, k, rows).items():
+        np.testing.assert_array_equal(a3[b].cpu().numpy(), ref)
+    for b, ref in _oracle_rows(s3, n3, k, rows, cand_pos=cp).items():
+        np.testing.assert_array_equal(a4[b].cpu().numpy(), ref)
 
 
 def test_noalloc_rejects_rows_beyond_its_scratch():
