@@ -32,7 +32,7 @@ EXPORTS = (
     "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_append_step_ratio",
     "csa2_swa_export", "csa2_swa_restore",
     "csa2_prefill_index_scores",
-    "csa2_prefill_group",
+    "csa2_prefill_group", "csa2_topk_noalloc", "csa2_debug_set_fault",
 )
 
 _c_p, _c_i32, _c_i64, _c_sz, _c_f = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -102,6 +102,7 @@ def lib() -> ctypes.CDLL:
     L.csa2_layer_group.argtypes = [ctypes.POINTER(GroupArgs), _c_p]
     L.csa2_prefill_index_scores.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p]
     L.csa2_prefill_group.argtypes = [ctypes.POINTER(PrefillArgs), _c_p]
+    L.csa2_debug_set_fault.argtypes = [_c_i32, _c_i64]
     L.csa2_append_step.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32,
                                    _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p]
     L.csa2_swa_export.argtypes = [ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32, _c_i32, _c_p, ctypes.POINTER(_c_p), _c_p]
@@ -167,6 +168,16 @@ def launch_count() -> int:
 
 def version() -> int:
     return int(lib().csa2_version())
+
+
+FAULT_NONE, FAULT_ATTN, FAULT_SCAN, FAULT_PREFILL = 0, 1, 2, 3
+
+
+def debug_set_fault(fault: int, wait_ns: int = 0):
+    """Test hook (csa2_debug_set_fault): make later launches of one kernel
+    withhold a signal so that its bounded device waits run out, and set the
+    bound of every device wait (0 = the 2 s default)."""
+    _check(lib().csa2_debug_set_fault(int(fault), int(wait_ns)), "csa2_debug_set_fault")
 
 
 # ---- entry points ---------------------------------------------------------------

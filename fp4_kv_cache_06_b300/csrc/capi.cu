@@ -80,6 +80,12 @@ static bool attn_layers(AttnLayers* lay, const void* const* q, const void* const
 // ---- bookkeeping --------------------------------------------------------------
 static std::atomic<uint64_t> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// Test hook: see csa2_debug_set_fault.
+static std::atomic<int> g_fault{kFaultNone};
+static std::atomic<uint64_t> g_wait_ns{2000000000ull};
+int debug_fault() { return g_fault.load(std::memory_order_relaxed); }
+uint64_t debug_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 int launch_status() { return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
 // Kernel attributes (dynamic shared memory above 48 KB) are set once per
@@ -206,9 +212,16 @@ const char* csa2_status_string(int status) {
   }
 }
 
-int csa2_version(void) { return 101; }
+int csa2_version(void) { return 102; }
 
 uint64_t csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int csa2_debug_set_fault(int32_t fault, int64_t wait_ns) {
+  if (fault < kFaultNone || fault > kFaultPrefill || wait_ns < 0) return CSA2_ERR_INVALID_ARG;
+  g_fault.store(fault, std::memory_order_relaxed);
+  g_wait_ns.store(wait_ns > 0 ? (uint64_t)wait_ns : 2000000000ull, std::memory_order_relaxed);
+  return CSA2_OK;
+}
 
 size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k, int32_t P, int32_t H) {
   if (B < 0 || n_max < 0) return 0;

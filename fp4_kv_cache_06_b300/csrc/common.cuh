@@ -34,6 +34,11 @@ constexpr int kBlock = 8;              // positions per pool block
 
 // ---- host bookkeeping ------------------------------------------------------
 void count_launch();
+// Test hook (csa2_debug_set_fault): a kernel that must never be signalled
+// once, and the bound of every device wait in nanoseconds.
+constexpr int kFaultNone = 0, kFaultAttn = 1, kFaultScan = 2, kFaultPrefill = 3;
+int debug_fault();
+uint64_t debug_wait_ns();
 int launch_status();                   // CSA2_OK or CSA2_ERR_CUDA after a launch
 // After a launch that returned `e`: also clears the runtime's last error.
 inline int launch_status(cudaError_t e) {

@@ -12,7 +12,7 @@
 namespace csa2 {
 
 constexpr int kD = 512;          // main head dim
-constexpr int kTile = 64;        // keys per tile of the attention kernel
+constexpr int kTile = 128;       // keys per tile of the attention kernel
 
 // Log-sum-exp merge of split-K partials. Partial O is stored
 // [layer][b][split][dim / 4][H][4] and (m, l) as [layer][b][split][H][2]
@@ -79,10 +79,12 @@ __global__ void __launch_bounds__(128) k_attn_merge(const float* __restrict__ pa
 int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                           int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
-                          float* part_ml, int splits, int tps, int32_t* st, cudaStream_t s);
+                          float* part_ml, int splits, int tps, int32_t* st, uint64_t wait_ns, int fault,
+                          cudaStream_t s);
 
 // Split-K count for `units` = rows x layers of one launch. The attention
-// kernel runs one CTA per SM (its shared memory and all 512 TMEM columns). A
+// kernel runs a pair of CTAs per unit and split, one CTA per SM (its shared
+// memory and all 512 TMEM columns), so kSMs / 2 units fit in a wave. A
 // launch that fills the machine runs unsplit (a split writes an fp32 partial
 // of H x 512 per CTA and needs the merge pass). Otherwise minimise
 // waves x tiles per split plus one tile-equivalent for the merge; ties go to
@@ -90,7 +92,7 @@ int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint
 int attn_splits(int64_t units, int H, int k, int W) {
   (void)H;
   const int n_tiles = (k + W + kTile - 1) / kTile;
-  const int64_t slots = kSMs;
+  const int64_t slots = kSMs / 2;
   if (units >= slots) return 1;
   const int64_t B = units;
   int best = 1;
@@ -145,7 +147,7 @@ int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t
   }
   int rc = launch_sparse_attn_tc(lay, L, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa_seq_stride, W,
                                  swa_tail, rps < 1 ? 1 : rps, swa_len, softmax_scale, part_o, part_ml, splits, tps,
-                                 st, s);
+                                 st, debug_wait_ns(), debug_fault() == kFaultAttn ? 1 : 0, s);
   if (rc != CSA2_OK || splits == 1) return rc;
   const dim3 grid((unsigned)(((kD / 4) * H + 127) / 128), (unsigned)B, (unsigned)L);
   auto kern = splits <= 4 ? k_attn_merge<4> : splits <= 8 ? k_attn_merge<8> : k_attn_merge<16>;

@@ -78,6 +78,24 @@ CSA2_API int csa2_version(void);
  * (host-side counter; graph replays of captured launches are not counted). */
 CSA2_API uint64_t csa2_launch_count(void);
 
+/* ---- test hook: bounded device waits -------------------------------------- */
+/* Every wait inside the kernels (on a tile, an accumulator, or the other CTA
+ * of a pair) gives up after a bound, reports CSA2_ERR_TIMEOUT through
+ * d_status, releases what the CTA holds (tensor memory) and returns; nothing
+ * hangs or traps. This hook lets tests exercise that path without faulting
+ * the GPU: with `fault` != CSA2_FAULT_NONE, every later launch of that kernel
+ * withholds one signal (its producers never hand over their last tile), so
+ * its consumers' waits run out. `wait_ns` sets the bound of every device wait
+ * (0 = the default, 2 s). Process-wide; not for production use. The pages
+ * have no counterpart: this exists to test the library's own failure path. */
+enum csa2_fault {
+  CSA2_FAULT_NONE = 0,
+  CSA2_FAULT_ATTN = 1,       /* sparse attention (csa2_sparse_attn, groups)  */
+  CSA2_FAULT_SCAN = 2,       /* Full indexer scan (TMA-fed form)             */
+  CSA2_FAULT_PREFILL = 3     /* prefill indexer GEMM                         */
+};
+CSA2_API int csa2_debug_set_fault(int32_t fault, int64_t wait_ns);
+
 /* ---- workspace sizing -------------------------------------------------- */
 enum csa2_op {
   CSA2_OP_TOPK = 1,          /* csa2_topk                                  */
@@ -296,12 +314,14 @@ CSA2_API int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t
 /* out[b][h] = softmax(scale * q[b][h] . X^T) X over the keys X = the
  * dequantised main-KV rows idx[b][0..k) (-1 = absent; main K = V) followed
  * by the present rows of the sequence's SWA window (K = V, bf16).
- * Q.K^T and P.V run on the tcgen05 tensor cores with fp16 operands and fp32
- * accumulation (TMEM): the FP4 dequantisation (E2M1 x E4M3) is exact in
- * fp16, Q and SWA rows are converted from bf16 (exact for magnitudes
- * 2^-14 .. 65504, 2^-24 absolute below, saturating above), probabilities
- * are rounded to fp16. Key tiles beyond one CTA are split-K partials merged
- * by log-sum-exp. A row with no key at all gets zeros.
+ * Q.K^T and P.V run on the tcgen05 tensor cores with bf16 operands and fp32
+ * accumulation (TMEM), on a pair of CTAs that split the head dims. Every
+ * operand is exact: Q and SWA rows are the bf16 inputs themselves, and the
+ * FP4 dequantisation (E2M1 x E4M3, at most 6 significant bits) is exact in
+ * bf16; the probabilities are rounded to bf16 (the denominator sums the
+ * rounded values). Logits must be finite in fp32. Key tiles beyond one CTA
+ * pair are split-K partials merged by log-sum-exp. A row with no key at all
+ * gets zeros.
  *   q, out   [B][H][d] bf16
  *   codes/scales row (b,t) at (b*kv_seq_stride + t); t must be < n_cap
  *            (checked: CSA2_ERR_DEVICE_BOUNDS, key skipped)

@@ -112,3 +112,44 @@ def test_prefill_layout_shared_cache_and_sliding_rows():
     sb, qb = bits16(swa_rows), bits16(q)
     ref = np.stack([oracle.sparse_attention(qb[i], c, s, idx[i], sb[i:i + W], W) for i in range(Q)])
     check_attn(out, ref)
+
+
+def test_sparse_attn_exact_over_the_bf16_range():
+    """Queries and SWA rows far outside fp16's range (|x| up to 1e5) and far
+    below it (|x| ~ 1e-6), mixed per head and per row: the MMA operands are
+    the bf16 inputs themselves, so the result follows the float64 oracle
+    within the usual bound (2e-3 plus the bf16 rounding of the output)."""
+    B, H, k, n, W = 3, 64, 512, 2500, 128
+    kv, codes, scales = _cache(B, n, seed=77)
+    rng = np.random.default_rng(77)
+    idx = np.stack([np.sort(rng.permutation(n)[:k]) for _ in range(B)]).astype(np.int32)
+    g = torch.Generator().manual_seed(77)
+    head_scale = torch.tensor([1e5 if h % 3 == 0 else (1e-6 if h % 3 == 1 else 1.0) for h in range(H)])
+    row_scale = torch.tensor([1e5 if r % 4 == 0 else (1e-6 if r % 4 == 1 else 1.0) for r in range(W)])
+    q = (torch.randn((B, H, 512), generator=g) * head_scale[None, :, None]).to(torch.bfloat16).to(DEV)
+    swa = (torch.randn((B, W, 512), generator=g) * row_scale[None, :, None]).to(torch.bfloat16).to(DEV)
+    swa_len = torch.tensor([W, 77, 1], dtype=torch.int32, device=DEV)
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa, swa_len, out, ws)
+    torch.cuda.synchronize()
+    kvb, qb, swab = bits16(kv), bits16(q), bits16(swa)
+    ref = np.zeros((B, H, 512))
+    for b in range(B):
+        c, s = oracle.quantize_fp4(kvb[b])
+        ref[b] = oracle.sparse_attention(qb[b], c, s, idx[b], swab[b], int(swa_len[b]))
+    assert np.abs(ref).max() > 1e4                 # some outputs are dominated by the large rows
+    # heads with |q| ~ 1e5 have one-hot softmaxes: P is exactly 1 and 0, so
+    # the output is a key row itself and the strict bound applies
+    big = np.arange(H) % 3 == 0
+    hb, hs = torch.from_numpy(np.nonzero(big)[0]).to(DEV), torch.from_numpy(np.nonzero(~big)[0]).to(DEV)
+    check_attn(out[:, hb], ref[:, big])
+    # elsewhere large rows carry weight, and rounding P to bf16 moves the
+    # output by up to 2^-9 max_j |v_jd| per dim (the bound the library states)
+    vmax = np.zeros((B, 1, 512))
+    for b in range(B):
+        c, s = oracle.quantize_fp4(kvb[b])
+        sel = idx[b][idx[b] >= 0]
+        vmax[b, 0] = vmax_of(np.concatenate([oracle.dequant_fp4(c[sel], s[sel]),
+                                             oracle.bf16_bits_to_f64(swab[b][:int(swa_len[b])])]))
+    check_attn(out[:, hs], ref[:, ~big], vmax=vmax)
