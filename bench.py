@@ -50,6 +50,19 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the measured cuBLAS burst, else the fallback."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    except Exception:
+        return 1800.0, "fallback"
+
+
+FP4_ROW_BYTES = 288          # 256 B of E2M1 codes + 32 B of E4M3 scales per main-KV row
+SWA_ROW_BYTES = 1024         # one bf16 row of 512
+
+
 # ---------------------------------------------------------------------------
 # distributed plumbing (replicas only)
 # ---------------------------------------------------------------------------
@@ -367,6 +380,69 @@ class DecodeWorkload:
             l0 += L
         self.step_i += 1
 
+    def alg_bytes(self):
+        """Algorithmic bytes of one step by kind (the roofline numerators):
+        indexer keys of every Full scan, block means of every pool formed on
+        the mean-key rule, the pool slots of every Reindex scan, and, per
+        layer, the gathered FP4 rows and the SWA rows."""
+        cfg, B = self.cfg, self.B
+        n = min(self.n_end, self.n_cap)
+        d_I = cfg.d_I
+        out = {"indexer_keys": 0, "block_means": 0, "pool_slots": 0}
+        for mode, n_reuse, form_pool in cfg.groups:
+            if mode == "full":
+                out["indexer_keys"] += B * n * d_I
+            if form_pool and not (mode == "full" and self.pool_rule == "max"):
+                out["block_means"] += B * ((n + 7) // 8) * d_I
+            if mode == "reindex":
+                out["pool_slots"] += B * cfg.P * 8 * d_I
+        out["gather"] = self.layers * B * cfg.k * FP4_ROW_BYTES
+        out["swa"] = self.layers * B * cfg.W * SWA_ROW_BYTES
+        return out
+
+    def attn_launch_bytes(self, n_layers):
+        """Algorithmic bytes of one attention launch over n_layers layers
+        (each layer's gathered rows and SWA rows, as in alg_bytes)."""
+        return n_layers * self.B * (self.cfg.k * FP4_ROW_BYTES + self.cfg.W * SWA_ROW_BYTES)
+
+    def attn_launch_flops(self, n_layers):
+        """4 H (k + W) d flops per row and layer (S and PV)."""
+        return 4.0 * n_layers * self.B * self.cfg.H * (self.cfg.k + self.cfg.W) * 512
+
+    def step_layerwise(self, events=None):
+        """The same step with one attention launch per layer, each after the
+        previous one (the schedule of a model whose next layer's query
+        depends on this layer's output): the group call attends its first
+        layer, then csa2_sparse_attn attends each Reuse layer. `events` as in
+        step(); event 3 + l follows layer l's own launch."""
+        csa2, cfg = self.csa2, self.cfg
+        if self.step_i > 0 and self.cfg.steps > 1:
+            self.pos.add_(1)
+            self.n.add_(1)
+        csa2.csa2_append_step(self.kv_new, self.kI_new, self.swa_new, self.swa, self.pos, self.codes,
+                              self.scales, self.kI, self.kbar)
+        n_max = self.n_first + (self.cfg.steps - 1 if self.cfg.steps > 1 else 0)
+        n_max = min(n_max, self.n_cap)
+        l0 = 0
+        for g, (mode, n_reuse, form_pool) in enumerate(cfg.groups):
+            ev = None if events is None else events[g]
+            csa2.csa2_layer_group(
+                csa2.MODE_FULL if mode == "full" else csa2.MODE_REINDEX, self.n, n_max, self.codes, self.scales,
+                self.kI, self.qI[g], self.w[g], self.idx[g], self.q[l0:l0 + 1], self.swa[l0:l0 + 1], self.swa_len,
+                self.out[l0:l0 + 1], self.ws, kbar=self.kbar, pool=self.pool,
+                form_pool=self._rule(mode) if form_pool else csa2.POOL_NONE,
+                qI_pool=self.qI_pool if mode == "reindex" else None,
+                w_pool=self.w_pool if mode == "reindex" else None,
+                events=None if ev is None else ev[:4])
+            for r in range(n_reuse):
+                l = l0 + 1 + r
+                csa2.csa2_sparse_attn(self.q[l], self.codes, self.scales, self.idx[g], self.swa[l], self.swa_len,
+                                      self.out[l], self.ws)
+                if ev is not None:
+                    ev[4 + r].record()
+            l0 += 1 + n_reuse
+        self.step_i += 1
+
     def scan_positions(self):
         """Positions the Full scans of one step read (for the roofline)."""
         return sum(self.B * min(self.n_end, self.n_cap) for (m, _, _) in self.cfg.groups if m == "full")
@@ -374,8 +450,16 @@ class DecodeWorkload:
     tokens_per_step = property(lambda self: self.B)
 
     def scan_bytes(self, d_I):
-        """Algorithmic bytes of one Full-scan launch: every key once, one score per query row."""
-        return self.B * min(self.n_end, self.n_cap) * SCAN_BYTES_PER_POS(d_I)
+        """Algorithmic bytes of one Full-scan launch: every indexer key once."""
+        return self.B * min(self.n_end, self.n_cap) * d_I
+
+    def scan_score_bytes(self):
+        """The fp32 score the scan writes per query row and position."""
+        return self.B * min(self.n_end, self.n_cap) * 4
+
+    def pool_scan_bytes(self, d_I):
+        """Algorithmic bytes of one block-mean scan (pool formation)."""
+        return self.B * ((min(self.n_end, self.n_cap) + 7) // 8) * d_I
 
     # host-side step for the end-to-end figure: per-step inputs from pinned host memory
     def host_buffers(self):
@@ -436,7 +520,26 @@ class MultiTokenWorkload(DecodeWorkload):
     tokens_per_step = property(lambda self: self.rows)
 
     def scan_bytes(self, d_I):
-        return self.B * self.n_cap * d_I + self.rows * self.n_cap * 4
+        return self.B * self.n_cap * d_I                 # keys read once per sequence for its R rows
+
+    def scan_score_bytes(self):
+        return self.rows * self.n_cap * 4
+
+    def alg_bytes(self):
+        cfg, rows = self.cfg, self.rows
+        out = super().alg_bytes()
+        out["gather"] = self.layers * rows * cfg.k * FP4_ROW_BYTES
+        out["swa"] = self.layers * rows * cfg.W * SWA_ROW_BYTES
+        out["pool_slots"] = sum(rows * cfg.P * 8 * cfg.d_I for m, _, _ in cfg.groups if m == "reindex")
+        return out
+
+    def attn_launch_bytes(self, n_layers):
+        return n_layers * self.rows * (self.cfg.k * FP4_ROW_BYTES + self.cfg.W * SWA_ROW_BYTES)
+
+    def attn_launch_flops(self, n_layers):
+        return 4.0 * n_layers * self.rows * self.cfg.H * (self.cfg.k + self.cfg.W) * 512
+
+    step_layerwise = None
 
     def reset_positions(self):
         self.step_i = 0

@@ -32,7 +32,7 @@ EXPORTS = (
     "csa2_sparse_attn", "csa2_layer_group", "csa2_append_step", "csa2_append_step_ratio",
     "csa2_swa_export", "csa2_swa_restore",
     "csa2_prefill_index_scores",
-    "csa2_prefill_group", "csa2_topk_noalloc", "csa2_debug_set_fault",
+    "csa2_prefill_group", "csa2_topk_noalloc", "csa2_debug_set_fault", "csa2_last_cuda_error",
 )
 
 _c_p, _c_i32, _c_i64, _c_sz, _c_f = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
     L.csa2_prefill_index_scores.argtypes = [_c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_p]
     L.csa2_prefill_group.argtypes = [ctypes.POINTER(PrefillArgs), _c_p]
     L.csa2_debug_set_fault.argtypes = [_c_i32, _c_i64]
+    L.csa2_last_cuda_error.restype = ctypes.c_char_p
     L.csa2_append_step.argtypes = [_c_p, _c_p, ctypes.POINTER(_c_p), ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32,
                                    _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_p, _c_p]
     L.csa2_swa_export.argtypes = [ctypes.POINTER(_c_p), _c_i32, _c_i32, _c_i32, _c_i32, _c_p, ctypes.POINTER(_c_p), _c_p]
@@ -112,7 +113,8 @@ def lib() -> ctypes.CDLL:
                                          _c_i32, _c_i32, _c_i32, _c_p, _c_i32, _c_p, _c_p, _c_p, _c_p, _c_i64,
                                          _c_p, _c_p, _c_p, _c_p]
     for name in EXPORTS:
-        if name not in ("csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size"):
+        if name not in ("csa2_status_string", "csa2_version", "csa2_launch_count", "csa2_workspace_size",
+                        "csa2_last_cuda_error"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -130,7 +132,10 @@ def _stream(stream=None):
 
 def _check(rc: int, what: str):
     if rc != OK:
-        raise Csa2Error(f"{what}: {lib().csa2_status_string(rc).decode()}")
+        msg = f"{what}: {lib().csa2_status_string(rc).decode()}"
+        if rc == 4:                                   # CSA2_ERR_CUDA: add the CUDA error's text
+            msg += f" ({lib().csa2_last_cuda_error().decode()})"
+        raise Csa2Error(msg)
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim=None):

@@ -12,6 +12,7 @@
 // kernels on the caller's stream and returns a csa2_status; nothing here
 // synchronises the host or allocates device memory.
 #include <atomic>
+#include <cstdio>
 #include <mutex>
 
 #include "common.cuh"
@@ -86,7 +87,18 @@ static std::atomic<int> g_fault{kFaultNone};
 static std::atomic<uint64_t> g_wait_ns{2000000000ull};
 int debug_fault() { return g_fault.load(std::memory_order_relaxed); }
 uint64_t debug_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
-int launch_status() { return cudaGetLastError() == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+// The text of the last CUDA error a call of this thread ran into.
+static thread_local char g_cuda_error[160] = "";
+int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return CSA2_OK;
+  snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return CSA2_ERR_CUDA;
+}
+void note_cuda_error(cudaError_t e) {
+  if (e != cudaSuccess)
+    snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+}
 
 // Kernel attributes (dynamic shared memory above 48 KB) are set once per
 // device, on the first call that runs on it.
@@ -158,17 +170,21 @@ static int full_indexer(const uint8_t* qI, const float* w, const uint8_t* kI, in
   return launch_topk(scores, nullptr, n_max, n, 1, B, n_max, k, idx_out, tk, !shared_scan, s);
 }
 
+// e_begin / e_end (optional) are recorded around the block-mean scan alone.
 static int pool_indexer(const uint8_t* qI, const float* w, const uint8_t* kbar, int64_t kbar_seq_stride, int rps,
                         const int64_t* n, int B, int H_I, int d_I, int64_t n_max, int P, int32_t* pool_out,
-                        void* ws, int32_t* st, cudaStream_t s) {
+                        void* ws, int32_t* st, cudaStream_t s, cudaEvent_t e_begin = nullptr,
+                        cudaEvent_t e_end = nullptr) {
   int rc;
   const int64_t nb_max = (n_max + kBlock - 1) / kBlock;     // rows of block means
   float* scores = static_cast<float*>(ws);
   void* tk = static_cast<char*>(ws) + align256((size_t)B * (size_t)nb_max * 4);
   if ((rc = topk_prepare(tk, B, s)) != CSA2_OK) return rc;
+  if ((rc = rec(e_begin, s)) != CSA2_OK) return rc;
   if ((rc = launch_index_scan(qI, w, kbar, kbar_seq_stride, rps, n, kBlock, B, H_I, d_I, nb_max, scores, nb_max,
                               nullptr, 0, nullptr, topk_ws_hist(tk), topk_ws_hdr(tk, B), P, st, s)) != CSA2_OK)
     return rc;
+  if ((rc = rec(e_end, s)) != CSA2_OK) return rc;
   return launch_topk(scores, nullptr, nb_max, n, kBlock, B, nb_max, P, pool_out, tk, true, s);
 }
 
@@ -208,6 +224,7 @@ const char* csa2_status_string(int status) {
     case CSA2_ERR_CUDA: return "CSA2_ERR_CUDA";
     case CSA2_ERR_TIMEOUT: return "CSA2_ERR_TIMEOUT";
     case CSA2_ERR_DEVICE_BOUNDS: return "CSA2_ERR_DEVICE_BOUNDS";
+    case CSA2_ERR_DEVICE_RANGE: return "CSA2_ERR_DEVICE_RANGE";
     default: return "CSA2_ERR_UNKNOWN";
   }
 }
@@ -215,6 +232,8 @@ const char* csa2_status_string(int status) {
 int csa2_version(void) { return 102; }
 
 uint64_t csa2_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* csa2_last_cuda_error(void) { return g_cuda_error; }
 
 int csa2_debug_set_fault(int32_t fault, int64_t wait_ns) {
   if (fault < kFaultNone || fault > kFaultPrefill || wait_ns < 0) return CSA2_ERR_INVALID_ARG;
@@ -497,13 +516,15 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
       rc = launch_pool_block_max(static_cast<const float*>(a->ws), a->n_max, a->n, a->B, a->n_max, a->P, a->pool,
                                  static_cast<char*>(a->ws) + ws_index_full(a->B, a->n_max), s);
   } else {
-    if ((rc = rec(group_event(a, 0), s)) != CSA2_OK) return rc;
+    // a Reindex group that forms the pool: events [0] / [1] bracket the
+    // block-mean scan (its largest kernel); otherwise the Reindex scan
     if (a->form_pool)
       rc = pool_indexer(qp, wp, a->kbar, nbc, rps, a->n, a->B, a->H_I, a->d_I, a->n_max, a->P, a->pool, a->ws,
-                        a->d_status, s);
+                        a->d_status, s, group_event(a, 0), group_event(a, 1));
     if (rc == CSA2_OK)
       rc = reindex_indexer(a->qI, a->w, a->kI, a->n_cap, rps, a->n, a->pool, a->P, a->B, a->H_I, a->d_I, a->k,
-                           a->idx, a->ws, a->d_status, s, nullptr, group_event(a, 1));
+                           a->idx, a->ws, a->d_status, s, a->form_pool ? nullptr : group_event(a, 0),
+                           a->form_pool ? nullptr : group_event(a, 1));
   }
   if (rc != CSA2_OK) return rc;
   if ((rc = rec(group_event(a, 2), s)) != CSA2_OK) return rc;

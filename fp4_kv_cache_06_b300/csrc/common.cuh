@@ -41,8 +41,10 @@ int debug_fault();
 uint64_t debug_wait_ns();
 int launch_status();                   // CSA2_OK or CSA2_ERR_CUDA after a launch
 // After a launch that returned `e`: also clears the runtime's last error.
+void note_cuda_error(cudaError_t e);    // keep the text of e for csa2_last_cuda_error
 inline int launch_status(cudaError_t e) {
   const int st = launch_status();
+  if (e != cudaSuccess) note_cuda_error(e);
   return e == cudaSuccess ? st : CSA2_ERR_CUDA;
 }
 

@@ -12,7 +12,7 @@
 namespace csa2 {
 
 constexpr int kD = 512;          // main head dim
-constexpr int kTile = 128;       // keys per tile of the attention kernel
+constexpr int kTile = 64;        // keys per tile of the attention kernel
 
 // Log-sum-exp merge of split-K partials. Partial O is stored
 // [layer][b][split][dim / 4][H][4] and (m, l) as [layer][b][split][H][2]
@@ -83,8 +83,7 @@ int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint
                           cudaStream_t s);
 
 // Split-K count for `units` = rows x layers of one launch. The attention
-// kernel runs a pair of CTAs per unit and split, one CTA per SM (its shared
-// memory and all 512 TMEM columns), so kSMs / 2 units fit in a wave. A
+// kernel runs one CTA per SM (its shared memory and all 512 TMEM columns). A
 // launch that fills the machine runs unsplit (a split writes an fp32 partial
 // of H x 512 per CTA and needs the merge pass). Otherwise minimise
 // waves x tiles per split plus one tile-equivalent for the merge; ties go to
@@ -92,7 +91,7 @@ int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint
 int attn_splits(int64_t units, int H, int k, int W) {
   (void)H;
   const int n_tiles = (k + W + kTile - 1) / kTile;
-  const int64_t slots = kSMs / 2;
+  const int64_t slots = kSMs;
   if (units >= slots) return 1;
   const int64_t B = units;
   int best = 1;

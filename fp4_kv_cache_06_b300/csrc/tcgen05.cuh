@@ -49,13 +49,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 // Waits for the phase with the given parity to complete. try_wait may
 // suspend the thread for a while on each poll, so the bound is on wall time
-// (2 s, read from %globaltimer) as well as on the number of polls. Returns
-// false on timeout; the caller reports CSA2_ERR_TIMEOUT and winds down.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit = (1u << 22)) {
+// (limit_ns, 2 s by default, read from %globaltimer) as well as on the number
+// of polls. Returns false on timeout; the caller reports CSA2_ERR_TIMEOUT and
+// winds down.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 0; i < limit; ++i) {
+  for (uint32_t i = 0; i < (1u << 24); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && globaltimer_ns() - t0 > 2000000000ull) return false;
+    if ((i & 63) == 63 && globaltimer_ns() - t0 > limit_ns) return false;
   }
   return false;
 }

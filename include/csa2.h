@@ -65,11 +65,18 @@ enum csa2_status {
   CSA2_ERR_WORKSPACE = 3,        /* workspace missing or too small           */
   CSA2_ERR_CUDA = 4,             /* a CUDA launch or memset failed           */
   CSA2_ERR_TIMEOUT = 5,          /* a bounded device wait gave up            */
-  CSA2_ERR_DEVICE_BOUNDS = 6     /* (device) an index/length was out of range */
+  CSA2_ERR_DEVICE_BOUNDS = 6,    /* (device) an index/length was out of range */
+  CSA2_ERR_DEVICE_RANGE = 7      /* (device) an input value outside the range the
+                                    kernel represents exactly (see the call)  */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
 CSA2_API const char* csa2_status_string(int status);
+
+/* Name and text of the last CUDA error that made a call of the calling
+ * host thread return CSA2_ERR_CUDA ("" if none; static per-thread storage,
+ * valid until that thread's next failing call). */
+CSA2_API const char* csa2_last_cuda_error(void);
 
 /* Library ABI version (major*100 + minor). */
 CSA2_API int csa2_version(void);
@@ -314,14 +321,18 @@ CSA2_API int csa2_index_reindex(const uint8_t* qI, const float* w, const uint8_t
 /* out[b][h] = softmax(scale * q[b][h] . X^T) X over the keys X = the
  * dequantised main-KV rows idx[b][0..k) (-1 = absent; main K = V) followed
  * by the present rows of the sequence's SWA window (K = V, bf16).
- * Q.K^T and P.V run on the tcgen05 tensor cores with bf16 operands and fp32
- * accumulation (TMEM), on a pair of CTAs that split the head dims. Every
- * operand is exact: Q and SWA rows are the bf16 inputs themselves, and the
- * FP4 dequantisation (E2M1 x E4M3, at most 6 significant bits) is exact in
- * bf16; the probabilities are rounded to bf16 (the denominator sums the
- * rounded values). Logits must be finite in fp32. Key tiles beyond one CTA
- * pair are split-K partials merged by log-sum-exp. A row with no key at all
- * gets zeros.
+ * Q.K^T and P.V run on the tcgen05 tensor cores with fp16 operands and fp32
+ * accumulation (TMEM). The FP4 dequantisation (E2M1 x E4M3, at most 6
+ * significant bits in 2^-10 .. 2688) is exact in fp16. Each query head is
+ * scaled by the power of two that brings its largest magnitude into
+ * [2^14, 2^15), which makes every bf16 query exact (the factor is folded into
+ * the head's softmax scale). An SWA row whose largest magnitude reaches 2^16
+ * is scaled by 2^-b (b <= 7), with its logits and probabilities scaled back
+ * exactly; rows reaching 2^23 saturate and set CSA2_ERR_DEVICE_RANGE. SWA
+ * values below 2^-14 keep an absolute accuracy of 2^-25. Probabilities are
+ * rounded to fp16 and the softmax denominator sums the rounded values; logits
+ * must be finite in fp32. Key tiles beyond one CTA are split-K partials
+ * merged by log-sum-exp. A row with no key at all gets zeros.
  *   q, out   [B][H][d] bf16
  *   codes/scales row (b,t) at (b*kv_seq_stride + t); t must be < n_cap
  *            (checked: CSA2_ERR_DEVICE_BOUNDS, key skipped)
@@ -381,7 +392,11 @@ typedef struct csa2_group_args {
   void* const* events;   /* optional HOST array of cudaEvent_t recorded on
                             the stream: [0] the indexer scan begins, [1] the
                             scan ends, [2] Top-K (and pool) done, [3 + l]
-                            layer l's attention done. Up to 8 layers are
+                            layer l's attention done. The scan is the Full
+                            scan, the Reindex scan, or, in a Reindex group
+                            that forms the pool, the block-mean scan (the
+                            pool's Top-K and the Reindex scan then fall
+                            between [1] and [2]). Up to 8 layers are
                             attended by one launch, so the events of the
                             layers in it are recorded together after it      */
   int32_t n_events;      /* length of `events` (0 = none)                     */

@@ -116,9 +116,12 @@ def test_prefill_layout_shared_cache_and_sliding_rows():
 
 def test_sparse_attn_exact_over_the_bf16_range():
     """Queries and SWA rows far outside fp16's range (|x| up to 1e5) and far
-    below it (|x| ~ 1e-6), mixed per head and per row: the MMA operands are
-    the bf16 inputs themselves, so the result follows the float64 oracle
-    within the usual bound (2e-3 plus the bf16 rounding of the output)."""
+    below it (|x| ~ 1e-6), mixed per head and per row. Each query head is
+    brought into fp16's range by an exact power of two folded into its
+    softmax scale, and SWA rows beyond it by one folded into their logits and
+    probabilities, so the result follows the float64 oracle within the usual
+    bound (2e-3 plus the bf16 rounding of the output); no range error is
+    reported."""
     B, H, k, n, W = 3, 64, 512, 2500, 128
     kv, codes, scales = _cache(B, n, seed=77)
     rng = np.random.default_rng(77)
@@ -131,8 +134,10 @@ def test_sparse_attn_exact_over_the_bf16_range():
     swa_len = torch.tensor([W, 77, 1], dtype=torch.int32, device=DEV)
     out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)
     ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
-    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa, swa_len, out, ws)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa, swa_len, out, ws, d_status=st)
     torch.cuda.synchronize()
+    assert st.item() == 0
     kvb, qb, swab = bits16(kv), bits16(q), bits16(swa)
     ref = np.zeros((B, H, 512))
     for b in range(B):
@@ -153,3 +158,21 @@ def test_sparse_attn_exact_over_the_bf16_range():
         vmax[b, 0] = vmax_of(np.concatenate([oracle.dequant_fp4(c[sel], s[sel]),
                                              oracle.bf16_bits_to_f64(swab[b][:int(swa_len[b])])]))
     check_attn(out[:, hs], ref[:, ~big], vmax=vmax)
+
+
+def test_sparse_attn_reports_swa_rows_beyond_its_range():
+    """An SWA row reaching 2^23 (past the 2^7 scale-down) is reported as
+    CSA2_ERR_DEVICE_RANGE; the call still completes."""
+    B, H, k, n, W = 1, 16, 64, 200, 128
+    kv, codes, scales = _cache(B, n, seed=78)
+    idx = torch.arange(k, dtype=torch.int32, device=DEV)[None]
+    q = synth.normal_bf16((B, H, 512), seed=78, stream="q").to(DEV)
+    swa = synth.normal_bf16((B, W, 512), seed=78, stream="swa").to(DEV)
+    swa[0, 3, 7] = 1e8
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa2.csa2_sparse_attn(q, codes, scales, idx, swa, torch.tensor([W], dtype=torch.int32, device=DEV), out, ws,
+                          d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 7

@@ -47,8 +47,8 @@ def _attn_case(B, H=64, k=512, n=3000, W=128, seed=31):
 
 @pytest.mark.parametrize("B", [2, 80])
 def test_attention_wait_runs_out_and_next_call_is_correct(B):
-    """B = 2 runs split-K (one tile per CTA pair, plus the merge kernel);
-    B = 80 fills the machine with unsplit pairs of five tiles each."""
+    """B = 2 runs split-K (one key tile per CTA, plus the merge kernel);
+    B = 80 runs unsplit CTAs of ten key tiles each."""
     H, k, W = 64, 512, 128
     kv, codes, scales, idx, q, swa, swa_len = _attn_case(B)
     ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
