@@ -471,14 +471,19 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       for (int x = 0; x < 32; ++x) m4[x & 3] = fmaxf(m4[x & 3], __uint_as_float(r[x]));
       float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, 16));
-      // the scale is positive, so the scaled maximum is the maximum of the scaled scores
-      const float mt = mh * sl;
+      // The running maximum m_run is kept in score units and every exponent
+      // is formed as (s - m_run) * scale: the subtraction is exact near the
+      // maximum, so the largest key gets exactly 1 however large the logits
+      // (forming s * scale - m_run * scale instead loses the rounding error of
+      // m_run * scale, which for huge logits overflows exp2). The reference is
+      // raised only when a tile exceeds it by more than 8 in log2 units
+      // (probabilities stay <= 256).
       float alpha = 1.f;
-      if (mt > m_run + 8.f) {                 // raise the reference only when needed
-        alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - mt);
-        m_run = mt;
+      if (mh > m_run && (m_run == -INFINITY || (mh - m_run) * sl > 8.f)) {
+        alpha = (m_run == -INFINITY) ? 0.f : exp2f((m_run - mh) * sl);
+        m_run = mh;
       }
-      const float nbase = (m_run == -INFINITY) ? 0.f : -m_run;
+      const float mref = (m_run == -INFINITY) ? 0.f : m_run;
       // P and O are free once PV(j - 1) has finished
       if (j > 0) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1, wait_ns) && ok;
       if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int x = 8 * c + 2 * u;
-          float p0 = exp2f(fmaf(__uint_as_float(r[x]), sl, nbase)), p1 = exp2f(fmaf(__uint_as_float(r[x + 1]), sl, nbase));
+          float p0 = exp2f((__uint_as_float(r[x]) - mref) * sl), p1 = exp2f((__uint_as_float(r[x + 1]) - mref) * sl);
           int b0 = 0, b1 = 0;
           if (kscaled) {                      // a scaled row's value enters PV as 2^-b v: its P as 2^b P
             b0 = (int)((bw[x >> 2] >> (8 * (x & 3))) & 0xFF);
@@ -611,7 +616,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   if (warp < kSoftWarps && lane < 16) {
     const int h = 16 * warp + lane;
     sL[h] = have_o ? l_tot : 0.f;
-    sMx[h] = have_o ? m_run : -INFINITY;
+    // the partials carry the maximum in log2 units (the merge's domain)
+    sMx[h] = (have_o && m_run != -INFINITY) ? m_run * (scale_log2 * sQScale[h]) : -INFINITY;
   }
   __syncthreads();
   if (warp < 8) {
