@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
     const __grid_constant__ CUtensorMap map_k, const uint8_t* __restrict__ qI, const float* __restrict__ w,
     int64_t kI_seq_stride, int rps, const int64_t* __restrict__ n, int len_div, int H_I, int64_t n_max, int tiles_per_cta,
     float* __restrict__ scores, int64_t scores_stride, uint32_t* __restrict__ hist, TopkHdr* __restrict__ hdr,
-    int topk_k, int32_t* st) {
+    int topk_k, int32_t* st, uint64_t wait_ns, int fault) {
   __shared__ uint32_t sh_hist[kHistBins];
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -215,10 +215,13 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
       tc::prefetch_tmap(&map_k);
       for (int i = 0;; ++i) {
         const int s = i % kTmaStages;
-        if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kTmaStages) & 1) ^ 1)) {
+        if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kTmaStages) & 1) ^ 1, wait_ns)) {
           report(st, CSA2_ERR_TIMEOUT);            // the consumers time out on the full barrier
           break;
         }
+        // fault injection (tests of the bounded waits): the second stage is
+        // never loaded nor signalled, so the consumers' wait on it runs out
+        if (fault && i == 1) break;
         const int64_t tile = dynamic ? (int64_t)atomicAdd(&hdr[b].cnt, 1u) : t0 + i;
         if (tile >= (dynamic ? tiles_b : t1)) {
           sTile[s] = -1;                           // no more tiles: an arrive without bytes
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
     const int r1 = warp * 16 + sg, r2 = r1 + 8;     // tile rows of fragment rows g and g+8
     for (int i = 0;; ++i) {
       const int s = i % kTmaStages;
-      const bool got = tc::mbar_wait(bar_full + 8 * s, (i / kTmaStages) & 1);
+      const bool got = tc::mbar_wait(bar_full + 8 * s, (i / kTmaStages) & 1, wait_ns);
       if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) report(st, CSA2_ERR_TIMEOUT);
         break;
@@ -342,7 +345,7 @@ int launch_index_scan(const uint8_t* qI, const float* w, const uint8_t* kI, int6
 #define CSA2_TMA_SCAN(R_)                                                                                  \
   k_index_scan_tma<R_><<<grid, kTmaThreads, kTmaSmem, s>>>(map, qI, w, kI_seq_stride, rps, n, len_div, H_I, \
                                                           n_max, tpc, scores, scores_stride, hist, hdr,     \
-                                                          topk_k, st)
+                                                          topk_k, st, debug_wait_ns(), debug_fault() == kFaultScan)
       if (R == 8) CSA2_TMA_SCAN(8);
       else if (R == 4) CSA2_TMA_SCAN(4);
       else if (R == 2) CSA2_TMA_SCAN(2);

@@ -58,7 +58,7 @@ struct PrefillSmem {
 __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(
     const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
     const float* __restrict__ w, int Q, int64_t n_keys, int tiles_per_cta, float* __restrict__ scores,
-    int64_t stride, int32_t* st) {
+    int64_t stride, int32_t* st, uint64_t wait_ns, int fault) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;
@@ -114,20 +114,27 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(
     tc::tma_load_2d(base + L::kQ, &map_q, 0, qt * kPN, bar_q);
     for (int i = 0; i < nt; ++i) {
       const int s = i % kPStages;
-      if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kPStages) & 1) ^ 1)) { report(st, CSA2_ERR_TIMEOUT); *s_abort = 1; break; }
+      if (!tc::mbar_wait(bar_empty + 8 * s, ((i / kPStages) & 1) ^ 1, wait_ns)) {
+        report(st, CSA2_ERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
       if (*s_abort) break;
+      // fault injection (tests of the bounded waits): the second tile is
+      // never loaded nor signalled, so the MMA issuer's wait on it runs out
+      if (fault && i == 1) break;
       tc::mbar_expect_tx(bar_full + 8 * s, kPTileBytes);
       tc::tma_load_2d(base + L::kA + s * kPTileBytes, &map_k, 0, (int)((t0 + i) * kPM), bar_full + 8 * s);
     }
   } else if (warp == 1 && lane == 0 && nt > 0) {
     // ---- MMA issuer
     const uint32_t idesc = tc::instr_desc(tc::kFmtE4M3, tc::kFmtE4M3, 0, 0, kPM, kPN);
-    bool ok = tc::mbar_wait(bar_q, 0);
+    bool ok = tc::mbar_wait(bar_q, 0, wait_ns);
     int issued = 0;
     for (int i = 0; ok && i < nt; ++i) {
       const int s = i % kPStages, acc = i & 1;
-      if (!tc::mbar_wait(bar_full + 8 * s, (i / kPStages) & 1)) { ok = false; break; }
-      if (!tc::mbar_wait(bar_tempty + 8 * acc, ((i >> 1) & 1) ^ 1)) { ok = false; break; }
+      if (!tc::mbar_wait(bar_full + 8 * s, (i / kPStages) & 1, wait_ns)) { ok = false; break; }
+      if (!tc::mbar_wait(bar_tempty + 8 * acc, ((i >> 1) & 1) ^ 1, wait_ns)) { ok = false; break; }
       if (*s_abort) { ok = false; break; }
       tc::tc_fence_after();
       const uint32_t a0 = base + L::kA + s * kPTileBytes, b0 = base + L::kQ;
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(
     // wind down: the last commit of each accumulator tells that its MMAs finished
     if (issued > 0) {
       const int last = issued - 1;
-      tc::mbar_wait(bar_tfull + 8 * (last & 1), (last >> 1) & 1);
+      tc::mbar_wait(bar_tfull + 8 * (last & 1), (last >> 1) & 1, wait_ns);
     }
   } else if (warp >= 2) {
     // ---- epilogue: lane = entry, columns = query*8 + head
@@ -153,7 +160,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(
     for (int i = 0; i < nt; ++i) {
       const int acc = i & 1;
       // warp-uniform decision: the TMEM loads below are warp-collective
-      const bool got = tc::mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1);
+      const bool got = tc::mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1, wait_ns);
       if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *s_abort != 0)) {
         if (lane == 0) { report(st, CSA2_ERR_TIMEOUT); *s_abort = 1; }
         break;
@@ -249,7 +256,8 @@ int launch_prefill_index(const uint8_t* qI, const float* w, int Q, const uint8_t
   const int tpc = (int)((ktiles + splits - 1) / splits);
   splits = (ktiles + tpc - 1) / tpc;
   dim3 grid((unsigned)splits, (unsigned)qtiles);
-  k_prefill_index<<<grid, kPThreads, PrefillSmem::kBytes, s>>>(mk, mq, w, Q, n_keys, tpc, scores, stride, st);
+  k_prefill_index<<<grid, kPThreads, PrefillSmem::kBytes, s>>>(mk, mq, w, Q, n_keys, tpc, scores, stride, st,
+                                                                debug_wait_ns(), debug_fault() == kFaultPrefill);
   count_launch();
   return launch_status();
 }

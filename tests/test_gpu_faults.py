@@ -117,6 +117,63 @@ def test_layer_group_attention_wait_runs_out_then_recovers():
         assert torch.equal(a, r)
 
 
+def test_full_scan_wait_runs_out_and_next_call_is_correct():
+    """The TMA-fed Full indexer scan: its producer withholds the second key
+    tile of every CTA, the MMA warps' wait on it runs out, and the next scan
+    on the stream reproduces the scores of a normal call."""
+    B, n, H_I, d_I = 4, 32768, 8, 128
+    seed = 51
+    kI = synth.indexer_keys_e4m3((B, n, d_I), seed).to(DEV)
+    qI = synth.normal_e4m3((B, H_I, d_I), seed, "qI").to(DEV)
+    w = synth.uniform_f32((B, H_I), seed, "w").to(DEV)
+    nt = torch.full((B,), n, dtype=torch.int64, device=DEV)
+    ref = torch.empty((B, n), dtype=torch.float32, device=DEV)
+    csa2.csa2_index_scores(qI, w, kI, nt, n, ref)
+    torch.cuda.synchronize()
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = torch.zeros_like(ref)
+    with _fault(csa2.FAULT_SCAN):
+        csa2.csa2_index_scores(qI, w, kI, nt, n, got, d_status=st)
+        torch.cuda.synchronize()
+    assert st.item() == TIMEOUT
+    st.zero_()
+    csa2.csa2_index_scores(qI, w, kI, nt, n, got, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(got, ref)
+    b = 2
+    o = oracle.indexer_scores(qI.cpu().numpy()[b], w.cpu().numpy()[b], kI.cpu().numpy()[b, :2048])
+    np.testing.assert_allclose(got.cpu().numpy()[b, :2048], o, rtol=2e-6, atol=1e-6)
+
+
+def test_prefill_gemm_wait_runs_out_and_next_call_is_correct():
+    """The tcgen05 FP8 prefill indexer GEMM: its TMA producer withholds the
+    second entry tile of every CTA, the MMA issuer's wait runs out, the CTA
+    releases its tensor memory, and the next call is correct."""
+    Q, n_keys = 1024, 8192
+    seed = 52
+    kI = synth.indexer_keys_e4m3((n_keys, 128), seed).to(DEV)
+    qI = synth.normal_e4m3((Q, 8, 128), seed, "qI").to(DEV)
+    w = synth.uniform_f32((Q, 8), seed, "w").to(DEV)
+    ref = torch.empty((Q, n_keys), dtype=torch.float32, device=DEV)
+    csa2.csa2_prefill_index_scores(qI, w, kI, ref)
+    torch.cuda.synchronize()
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = torch.zeros_like(ref)
+    with _fault(csa2.FAULT_PREFILL):
+        csa2.csa2_prefill_index_scores(qI, w, kI, got, d_status=st)
+        torch.cuda.synchronize()
+    assert st.item() == TIMEOUT
+    st.zero_()
+    csa2.csa2_prefill_index_scores(qI, w, kI, got, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(got, ref)
+    qq = 700
+    o = oracle.indexer_scores(qI.cpu().numpy()[qq], w.cpu().numpy()[qq], kI.cpu().numpy())
+    np.testing.assert_allclose(got.cpu().numpy()[qq], o, rtol=2e-6, atol=1e-6)
+
+
 def test_fault_hook_rejects_bad_arguments():
     with pytest.raises(csa2.Csa2Error, match="INVALID_ARG"):
         csa2.debug_set_fault(99, 0)
