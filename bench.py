@@ -1362,6 +1362,7 @@ def main():
             dt, desc = oracle_baseline(cfg)
             res["cpu_baseline"] = {"value": 1.0 / dt, "unit": UNIT, "cores": oracle_cores(), "kind": "oracle",
                                    "sample": desc}
+    if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

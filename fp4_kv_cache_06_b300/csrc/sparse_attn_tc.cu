@@ -97,6 +97,8 @@ constexpr int kBarSFull = 4;              // [2] S ready (tcgen05.commit)
 constexpr int kBarPFull = 6;              // P ready (one arrive after the softmax group's barrier)
 constexpr int kBarODone = 7;              // PV done (tcgen05.commit)
 constexpr int kBarFin = 8;                // every MMA of the CTA done (tcgen05.commit)
+constexpr int kBarQ = 9;                  // Q converted (every thread of the converting warps arrives)
+constexpr int kQWarps = kSoftWarps + 1;   // the softmax warps and the MMA warp convert Q
 
 __device__ __forceinline__ uint32_t kt_off(int row, int chunk) {     // chunk = 16-byte unit of 8 dims
   return (uint32_t)((chunk >> 3) * 8192 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
@@ -227,6 +229,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     tc::mbar_init(bar(kBarPFull), 1);
     tc::mbar_init(bar(kBarODone), 1);
     tc::mbar_init(bar(kBarFin), 1);
+    tc::mbar_init(bar(kBarQ), 32 * kQWarps);
     tc::fence_barrier_init();
     sMisc[1] = 0;
     sMisc[2] = 0;
@@ -295,22 +298,28 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   const uint32_t tmem = sMisc[0];
   pdl_trigger();                              // TMEM is held: the next kernel may start launching
   // Q -> fp16, one warp per head: scaled by 2^-a so that the head's largest
-  // magnitude lies in [2^14, 2^15) (heads >= H and all-zero heads: a = 0)
-  for (int h = warp; h < 64; h += kTThreads / 32) {
-    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-    if (h < H) {
-      v0 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane));
-      v1 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane + 32));
+  // magnitude lies in [2^14, 2^15) (heads >= H and all-zero heads: a = 0).
+  // The softmax warps and the MMA warp do this while the producers start on
+  // tile 0; tile 1 goes into key buffer 1 (the bf16 staging of Q) only after
+  // every converting warp has arrived on kBarQ, and S and the softmax wait
+  // for it too.
+  if (warp < kSoftWarps || warp == kMmaWarp) {
+    for (int h = warp < kSoftWarps ? warp : kSoftWarps; h < 64; h += kQWarps) {
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (h < H) {
+        v0 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane));
+        v1 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane + 32));
+      }
+      const uint32_t mx = __reduce_max_sync(0xffffffffu, bf16x16_max_mag(v0, v1));
+      const int a = mx == 0 ? 0 : min(max((int)(mx >> 7) - 127 - 14, -100), 100);
+      const float f = pow2f(-a);
+      *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane)) = bf16x8_to_f16x8_scaled(v0, f);
+      *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane + 32)) = bf16x8_to_f16x8_scaled(v1, f);
+      if (lane == 0) sQScale[h] = pow2f(a);
     }
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, bf16x16_max_mag(v0, v1));
-    const int a = mx == 0 ? 0 : min(max((int)(mx >> 7) - 127 - 14, -100), 100);
-    const float f = pow2f(-a);
-    *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane)) = bf16x8_to_f16x8_scaled(v0, f);
-    *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane + 32)) = bf16x8_to_f16x8_scaled(v1, f);
-    if (lane == 0) sQScale[h] = pow2f(a);
+    tc::fence_async_smem();
+    tc::mbar_arrive(bar(kBarQ));
   }
-  tc::fence_async_smem();
-  __syncthreads();
 
   // softmax threads (warps 0-3): head 16 warp + (lane & 15), key columns
   // 32 (lane >> 4) .. + 31 of a tile; l_run sums the thread's column half,
@@ -347,7 +356,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       const int buf = j & 1, slot = j % kRing;
       const uint32_t kv = base + L::kKV + buf * L::kKVBytes;
       unsigned char* kvp = sp + L::kKV + buf * L::kKVBytes;
-      if (j + 3 < nt && p < 64) row_sources(j + 3, p);
+      // key buffer 1 held the bf16 Q until the converting warps were done
+      if (j == 1 && !tc::mbar_wait(bar(kBarQ), 0, wait_ns)) {
+        report(st, CSA2_ERR_TIMEOUT);
+        sMisc[3] = 1;
+      }
       // the buffer is free once PV(j - 2) has finished
       if (j >= 2 && !tc::mbar_wait(bar(kBarKvEmpty + buf), ((j >> 1) - 1) & 1, wait_ns)) {
         report(st, CSA2_ERR_TIMEOUT);
@@ -420,6 +433,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       // tile j + 2's row sources were written in produce(j - 1), before this
       // call's opening barrier
       if (j + 2 < nt) prefetch(j + 2, cw, sb);
+      // the row sources of tile j + 3 last: the latency of their index loads
+      // then overlaps the next tile's wait for its key buffer
+      if (j + 3 < nt && p < 64) row_sources(j + 3, p);
       return true;
     };
     if (nt > 0) prefetch(0, cwA, sbA);
@@ -439,6 +455,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     // reference.
     const int h = 16 * warp + (lane & 15);
     const int half = lane >> 4;
+    if (!tc::mbar_wait(bar(kBarQ), 0, wait_ns)) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
     const float sl = scale_log2 * sQScale[h];               // the head's query was scaled by 2^-a
     for (int j = 0; j < nt; ++j) {
       if (named_or(kNbSoft, kSoftThreads, sMisc[3] != 0)) break;
@@ -562,34 +579,47 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         tc::mma_commit(bar(kBarODone));
         tc::mma_commit(bar(kBarKvEmpty + (j & 1)));
       };
-      auto issue_s = [&](int j) {
+      // S(j) in two halves of 16 K steps (dims 0..255, 256..511); the second
+      // half commits. Issuing MMAs blocks this thread while the tensor pipe
+      // is busy (a 32-instruction S holds it about 1 us), so PV is checked
+      // between the halves.
+      auto issue_s_half = [&](int j, int half_k) {
         const uint32_t kv = base + L::kKV + (j & 1) * L::kKVBytes;
 #pragma unroll 4
-        for (int ks = 0; ks < kTD / 16; ++ks) {
+        for (int ks = 16 * half_k; ks < 16 * half_k + 16; ++ks) {
           const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
           const uint64_t ad = tc::smem_desc(base + L::kQ + off, 16, 1024, tc::kSwizzle128B);
           const uint64_t bd = tc::smem_desc(kv + off, 16, 1024, tc::kSwizzle128B);
           tc::mma_f16(tmem + 64u * (j & 1), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
-        tc::mma_commit(bar(kBarSFull + (j & 1)));
+        if (half_k == 1) tc::mma_commit(bar(kBarSFull + (j & 1)));
       };
-      // Issue S(js) once its key tile is ready (and S(js - 2)'s softmax has
-      // handed over, i.e. PV(js - 2) was issued), and PV(jp) once its P is
-      // ready; whichever comes first. The polls share one time bound.
+      // PV(jp) goes first whenever its P is ready: it frees a key buffer for
+      // the producers and P for the next softmax, which both wait on it.
+      // S(js) is issued once its key tile is ready (and S(js - 2)'s softmax
+      // has handed over, i.e. PV(js - 2) was issued). The polls share one
+      // time bound.
       bool ok = true;
+      if (!tc::mbar_wait(bar(kBarQ), 0, wait_ns)) ok = false;
       int js = 0, jp = 0;
+      bool s_open = false;                    // the first half of S(js) has been issued
       uint64_t t0 = tc::globaltimer_ns();
       uint32_t polls = 0;
-      while (jp < nt) {
+      while (ok && jp < nt) {
         bool progressed = false;
-        if (js < nt && js <= jp + 1 && tc::mbar_test_wait(bar(kBarKvFull + (js & 1)), (js >> 1) & 1)) {
-          tc::tc_fence_after();
-          issue_s(js++);
-          progressed = true;
-        }
         if (jp < js && tc::mbar_test_wait(bar(kBarPFull), jp & 1)) {
           tc::tc_fence_after();
           issue_pv(jp++);
+          progressed = true;
+        }
+        if (s_open) {
+          issue_s_half(js++, 1);
+          s_open = false;
+          progressed = true;
+        } else if (js < nt && js <= jp + 1 && tc::mbar_test_wait(bar(kBarKvFull + (js & 1)), (js >> 1) & 1)) {
+          tc::tc_fence_after();
+          issue_s_half(js, 0);
+          s_open = true;
           progressed = true;
         }
         if (progressed) {
