@@ -579,47 +579,35 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         tc::mma_commit(bar(kBarODone));
         tc::mma_commit(bar(kBarKvEmpty + (j & 1)));
       };
-      // S(j) in two halves of 16 K steps (dims 0..255, 256..511); the second
-      // half commits. Issuing MMAs blocks this thread while the tensor pipe
-      // is busy (a 32-instruction S holds it about 1 us), so PV is checked
-      // between the halves.
-      auto issue_s_half = [&](int j, int half_k) {
+      auto issue_s = [&](int j) {
         const uint32_t kv = base + L::kKV + (j & 1) * L::kKVBytes;
 #pragma unroll 4
-        for (int ks = 16 * half_k; ks < 16 * half_k + 16; ++ks) {
+        for (int ks = 0; ks < kTD / 16; ++ks) {
           const uint32_t off = (ks >> 2) * 8192 + (ks & 3) * 32;
           const uint64_t ad = tc::smem_desc(base + L::kQ + off, 16, 1024, tc::kSwizzle128B);
           const uint64_t bd = tc::smem_desc(kv + off, 16, 1024, tc::kSwizzle128B);
           tc::mma_f16(tmem + 64u * (j & 1), ad, bd, idesc_s, ks > 0 ? 1u : 0u);
         }
-        if (half_k == 1) tc::mma_commit(bar(kBarSFull + (j & 1)));
+        tc::mma_commit(bar(kBarSFull + (j & 1)));
       };
-      // PV(jp) goes first whenever its P is ready: it frees a key buffer for
-      // the producers and P for the next softmax, which both wait on it.
-      // S(js) is issued once its key tile is ready (and S(js - 2)'s softmax
-      // has handed over, i.e. PV(js - 2) was issued). The polls share one
-      // time bound.
+      // Issue S(js) once its key tile is ready (and S(js - 2)'s softmax has
+      // handed over, i.e. PV(js - 2) was issued), and PV(jp) once its P is
+      // ready; whichever comes first. The polls share one time bound.
       bool ok = true;
       if (!tc::mbar_wait(bar(kBarQ), 0, wait_ns)) ok = false;
       int js = 0, jp = 0;
-      bool s_open = false;                    // the first half of S(js) has been issued
       uint64_t t0 = tc::globaltimer_ns();
       uint32_t polls = 0;
       while (ok && jp < nt) {
         bool progressed = false;
+        if (js < nt && js <= jp + 1 && tc::mbar_test_wait(bar(kBarKvFull + (js & 1)), (js >> 1) & 1)) {
+          tc::tc_fence_after();
+          issue_s(js++);
+          progressed = true;
+        }
         if (jp < js && tc::mbar_test_wait(bar(kBarPFull), jp & 1)) {
           tc::tc_fence_after();
           issue_pv(jp++);
-          progressed = true;
-        }
-        if (s_open) {
-          issue_s_half(js++, 1);
-          s_open = false;
-          progressed = true;
-        } else if (js < nt && js <= jp + 1 && tc::mbar_test_wait(bar(kBarKvFull + (js & 1)), (js >> 1) & 1)) {
-          tc::tc_fence_after();
-          issue_s_half(js, 0);
-          s_open = true;
           progressed = true;
         }
         if (progressed) {
