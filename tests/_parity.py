@@ -42,12 +42,14 @@ def check_topk(gpu_idx, oracle_idx, oracle_scores, oracle_pos, k, band=TOPK_BAND
     return len(diff)
 
 
-# With few keys the weights p_j are large: rounding each p_j to bf16
-# (2^-9 relative) moves the output by up to 2^-9 * max_j |v_jd| per dim d,
-# and rounding the output itself adds 2^-9 * |o_d|. The absolute bounds
-# above assume hundreds of keys, where these errors average out; tests with
-# few keys pass vmax (per-dim max |v| over the keys) to add these terms.
-BF16_REL = 2.0 ** -9
+# bf16 carries an 8-bit significand, so rounding to bf16 moves a value by
+# up to 2^-8 of its magnitude (half an ulp just above a power of two).
+# With few keys the weights p_j are large: rounding each p_j moves the
+# output by up to 2^-8 * max_j |v_jd| per dim d, and rounding the output
+# itself adds 2^-8 * |o_d|. The absolute bounds above assume hundreds of
+# keys, where these errors average out; tests with few keys pass vmax
+# (per-dim max |v| over the keys) to add these terms.
+BF16_REL = 2.0 ** -8
 
 
 def vmax_of(keys):
@@ -58,9 +60,9 @@ def vmax_of(keys):
 
 def check_attn(gpu_out, oracle_out, max_abs=ATTN_MAX_ABS, mean_abs=ATTN_MEAN_ABS, vmax=None):
     """max-abs / mean-abs parity of bf16 outputs against float64. The max-abs
-    bound applies on top of the output format's own rounding: a bf16 output
-    cannot be closer to the exact value than half an ulp (2^-9 |ref|), which
-    alone reaches 2e-3 at |ref| ~ 0.5."""
+    bound applies on top of the output format's own rounding: a correctly
+    rounded bf16 output may sit half an ulp (up to 2^-8 |ref|) from the exact
+    value, which alone reaches 2e-3 at |ref| ~ 0.5."""
     g = bf16_to_f64(gpu_out)
     r = np.asarray(oracle_out)
     d = np.abs(g - r)
@@ -71,6 +73,39 @@ def check_attn(gpu_out, oracle_out, max_abs=ATTN_MAX_ABS, mean_abs=ATTN_MEAN_ABS
     assert np.all(d <= bound), (f"abs err {d.flat[worst]:.3e} > bound {np.broadcast_to(bound, d.shape).flat[worst]:.3e} "
                                 f"at |ref| {abs(r.flat[worst]):.4f} (gpu {g.flat[worst]:.6f}, max err {d.max():.3e}, "
                                 f"mean err {d.mean():.3e}, max |ref| {np.abs(r).max():.3f})")
+    # the mean is taken against the oracle rounded to bf16, so that the
+    # output format's own rounding (2^-9 |ref| on average, which outgrows the
+    # bound once |ref| is near 1, as with windows of repeated rows) is not
+    # counted as error
+    rb = torch.from_numpy(np.ascontiguousarray(r, dtype=np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
+    dm = np.abs(g - np.broadcast_to(rb, g.shape))
     mbound = mean_abs + (0.0 if vmax is None else float(np.mean(extra)))
-    assert d.mean() <= mbound, f"mean abs err {d.mean():.3e} > {mbound:.3e}"
-    return float(d.max()), float(d.mean())
+    assert dm.mean() <= mbound, f"mean abs err {dm.mean():.3e} > {mbound:.3e} (vs unrounded {d.mean():.3e})"
+    return float(d.max()), float(dm.mean())
+
+
+def attn_with_oracle_idx(q_row, codes_seq, scales_seq, oracle_idx, swa_rows, W=128):
+    """Sparse attention for one row on the GPU with the oracle's Top-K as its
+    index list (an input that comes from the oracle, never the reverse).
+
+    Used where the kernel's own selection legitimately differs from the
+    oracle's inside the tie band: the attention of that row is then still
+    compared, over the entries the oracle chose. q_row [H][512] bf16;
+    codes_seq [n][256], scales_seq [n][32] u8 (device); oracle_idx [k] ints
+    (-1 padded); swa_rows [s][512] bf16 with s <= W. Returns [1][H][512]."""
+    from fp4_kv_cache_06_b300 import csa2
+    dev = codes_seq.device
+    H = q_row.shape[0]
+    k = len(oracle_idx)
+    s = swa_rows.shape[0]
+    swa = torch.zeros((1, W, 512), dtype=torch.bfloat16, device=dev)
+    swa[0, :s] = swa_rows.to(dev)
+    idx = torch.from_numpy(np.asarray(oracle_idx, dtype=np.int32)[None].copy()).to(dev)
+    out = torch.empty((1, H, 512), dtype=torch.bfloat16, device=dev)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, 1, 0, k, 2048, H), dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    csa2.csa2_sparse_attn(q_row[None].to(dev), codes_seq[None], scales_seq[None], idx, swa,
+                          torch.tensor([s], dtype=torch.int32, device=dev), out, ws, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return out

@@ -21,7 +21,7 @@ import torch
 import oracle
 import synth
 from fp4_kv_cache_06_b300 import csa2
-from tests._parity import bits16, check_attn, check_topk, u8
+from tests._parity import attn_with_oracle_idx, bits16, check_attn, check_topk, u8
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -59,16 +59,51 @@ def _oracle_rows(base_b):
     return oracle.quantize_fp4(bits16(base_b))
 
 
-_compared = {"n": 0}
+_compared = {"group": 0, "oracle_idx": 0}
+
+
+def _reset():
+    _compared["group"] = 0
+    _compared["oracle_idx"] = 0
 
 
 def _check_attention(out_b, q_b, swa_b, c, s, idx):
     """out_b [1][H][512] from the kernel; the oracle attends over rows idx mod R."""
-    _compared["n"] += 1
     idx = np.asarray(idx)
     rows = np.where(idx >= 0, idx % R, -1)
     ref = oracle.sparse_attention(bits16(q_b), c, s, rows, bits16(swa_b), 128)
     check_attn(out_b, ref[None])
+
+
+def _check_layers(b, gpu_idx, ref_idx, outs, qs, swas, codes, scales, c, s, layers):
+    """Attention parity of sequence b's layers. Where the kernel's selection
+    equals the oracle's, the group's own outputs are compared; where it
+    differs inside the tie band, the row is attended again on the GPU over
+    the oracle's entries and that output is compared."""
+    same = np.array_equal(gpu_idx, ref_idx)
+    for l in layers:
+        if same:
+            got = outs[l][b:b + 1]
+            _compared["group"] += 1
+        else:
+            got = attn_with_oracle_idx(qs[l][b], codes[b], scales[b], ref_idx, swas[l][b])
+            _compared["oracle_idx"] += 1
+        _check_attention(got, qs[l][b], swas[l][b], c, s, ref_idx)
+
+
+def _reindex_with_pool(qI_b, w_b, kI_b, n, pool_row, k=512):
+    """The Reindex scan and Top-K of one sequence on the GPU over a given pool
+    (the oracle's, where the kernel's pool differs inside the tie band)."""
+    idx = torch.empty((1, k), dtype=torch.int32, device=DEV)
+    P = len(pool_row)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_INDEX_REINDEX, 1, n, k, P, 64))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa2.csa2_index_reindex(qI_b[None].to(DEV), w_b[None].to(DEV), kI_b[None], torch.tensor([n], device=DEV),
+                            torch.from_numpy(np.asarray(pool_row, dtype=np.int32)[None].copy()).to(DEV), k, idx, ws,
+                            d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return idx.cpu().numpy()[0]
 
 
 def _group(mode, n_t, n_max, codes, scales, kI, qI, w, qs, swas, kbar, pool, form_pool, qP=None, wP=None,
@@ -98,8 +133,9 @@ def _full_state(B, n, bias):
 
 
 def test_decoder_group_full_b32_ctx131072_sampled():
-    """Full + 3 Reuse, batch 32, 131,072 positions, 5 % biased keys."""
-    _compared["n"] = 0
+    """Full + 3 Reuse, batch 32, 131,072 positions, 5 % biased keys: eight
+    sampled sequences, every layer of each compared."""
+    _reset()
     cfg = synth.get_config(2)
     B, n, H, L = cfg.B, cfg.n, cfg.H, 4
     base, codes, scales, kI, kbar, n_t, pool = _full_state(B, n, cfg.bias_prob)
@@ -108,20 +144,19 @@ def test_decoder_group_full_b32_ctx131072_sampled():
     qs, swas = _layer_inputs(B, H, L)
     gi, outs = _group(csa2.MODE_FULL, n_t, n, codes, scales, kI, qI.to(DEV), w.to(DEV), qs, swas, kbar, pool,
                       False)
-    for b in (0, 13, 31):
+    sample = (0, 4, 9, 13, 18, 22, 27, 31)
+    for b in sample:
         ref_idx, ref_s = oracle.full_topk(u8(qI)[b], w.numpy()[b], _keys_host(b, n, cfg.bias_prob), n)
         check_topk(gi[b], ref_idx, ref_s, np.arange(n), 512)
-        if not np.array_equal(gi[b], ref_idx):
-            continue
         c, s = _oracle_rows(base[b])
-        for l in range(L):
-            _check_attention(outs[l][b:b + 1], qs[l][b], swas[l][b], c, s, ref_idx)
-    assert _compared["n"] >= 8, "too few sampled sequences had the oracle's exact Top-K"
+        _check_layers(b, gi[b], ref_idx, outs, qs, swas, codes, scales, c, s, range(L))
+    assert _compared["group"] + _compared["oracle_idx"] == len(sample) * L
+    assert _compared["group"] >= len(sample) * L // 2, _compared
 
 
 def test_decoder_group_pool_reindex_b8_ctx1m_sampled():
     """Pool formation + Reindex + 3 Reuse, batch 8, 1,048,576 positions."""
-    _compared["n"] = 0
+    _reset()
     cfg = synth.get_config(3)
     B, n, H, L, P = cfg.B, cfg.n, cfg.H, 4, cfg.P
     base, codes, scales, kI, kbar, n_t, pool = _full_state(B, n, 0.0)
@@ -133,28 +168,27 @@ def test_decoder_group_pool_reindex_b8_ctx1m_sampled():
     gi, outs = _group(csa2.MODE_REINDEX, n_t, n, codes, scales, kI, qI.to(DEV), w.to(DEV), qs, swas, kbar, pool,
                       True, qP=qP.to(DEV), wP=wP.to(DEV), P=P)
     gp = pool.cpu().numpy()
-    for b in (0, 7):
+    sample = (0, 7)
+    for b in sample:
         kb = _keys_host(b, n, 0.0)
         kbar_ref = oracle.block_means(kb, n)
         ref_pool, ref_bs = oracle.form_pool(u8(qP)[b], wP.numpy()[b], kbar_ref, P)
         check_topk(gp[b], ref_pool, ref_bs, np.arange(kbar_ref.shape[0]), P)
-        if not np.array_equal(gp[b], ref_pool):
-            continue
         ref_idx, ref_s, ref_pos = oracle.reindex_topk(u8(qI)[b], w.numpy()[b], kb, ref_pool, n)
-        check_topk(gi[b], ref_idx, ref_s, ref_pos, 512)
-        if not np.array_equal(gi[b], ref_idx):
-            continue
+        # the Reindex selection: the group's where its pool is the oracle's,
+        # else the GPU Reindex run again over the oracle's pool
+        g_idx = gi[b] if np.array_equal(gp[b], ref_pool) else _reindex_with_pool(qI[b], w[b], kI[b], n, ref_pool)
+        check_topk(g_idx, ref_idx, ref_s, ref_pos, 512)
         c, s = _oracle_rows(base[b])
-        for l in range(L):
-            _check_attention(outs[l][b:b + 1], qs[l][b], swas[l][b], c, s, ref_idx)
-    assert _compared["n"] >= 4, "too few sampled sequences had the oracle's exact pool and Top-K"
+        _check_layers(b, gi[b], ref_idx, outs, qs, swas, codes, scales, c, s, range(L))
+    assert _compared["group"] + _compared["oracle_idx"] == len(sample) * L
 
 
 def test_decoder_stack_b4_ctx1m_sampled():
     """The 20-layer stack's groups at 1,048,576 positions, batch 4: Full + 3
     Reuse forming the pool with the Full layer's indexer query, then four
     Reindex + 3 Reuse groups over that pool."""
-    _compared["n"] = 0
+    _reset()
     cfg = synth.get_config(5)
     B, n, H = cfg.B, cfg.n, cfg.H
     base, codes, scales, kI, kbar, n_t, pool = _full_state(B, n, 0.0)
@@ -172,7 +206,8 @@ def test_decoder_stack_b4_ctx1m_sampled():
         results.append((mode, gi, outs, qs, swas))
         l0 += L
     gp = pool.cpu().numpy()
-    for b in (0, 3):
+    sample = (0, 3)
+    for b in sample:
         kb = _keys_host(b, n, 0.0)
         c, s = _oracle_rows(base[b])
         # group 0: Full Top-512 and the pool formed with the same indexer query
@@ -181,18 +216,16 @@ def test_decoder_stack_b4_ctx1m_sampled():
         kbar_ref = oracle.block_means(kb, n)
         ref_pool, ref_bs = oracle.form_pool(u8(qIs[0])[b], ws_[0].numpy()[b], kbar_ref, cfg.P)
         check_topk(gp[b], ref_pool, ref_bs, np.arange(kbar_ref.shape[0]), cfg.P)
-        if np.array_equal(results[0][1][b], ref_idx):
-            _check_attention(results[0][2][0][b:b + 1], results[0][3][0][b], results[0][4][0][b], c, s, ref_idx)
-        if not np.array_equal(gp[b], ref_pool):
-            continue
+        _, gi, outs, qs, swas = results[0]
+        _check_layers(b, gi[b], ref_idx, outs, qs, swas, codes, scales, c, s, (0, len(outs) - 1))
+        same_pool = np.array_equal(gp[b], ref_pool)
         for g in range(1, G):
             ref_idx, ref_s, ref_pos = oracle.reindex_topk(u8(qIs[g])[b], ws_[g].numpy()[b], kb, ref_pool, n)
             _, gi, outs, qs, swas = results[g]
-            check_topk(gi[b], ref_idx, ref_s, ref_pos, 512)
-            if np.array_equal(gi[b], ref_idx):
-                last = len(outs) - 1
-                _check_attention(outs[last][b:b + 1], qs[last][b], swas[last][b], c, s, ref_idx)
-    assert _compared["n"] >= 6, "too few sampled sequences had the oracle's exact Top-K"
+            g_idx = gi[b] if same_pool else _reindex_with_pool(qIs[g][b], ws_[g][b], kI[b], n, ref_pool)
+            check_topk(g_idx, ref_idx, ref_s, ref_pos, 512)
+            _check_layers(b, gi[b], ref_idx, outs, qs, swas, codes, scales, c, s, (len(outs) - 1,))
+    assert _compared["group"] + _compared["oracle_idx"] == len(sample) * (2 + (G - 1))
 
 
 def test_encoder_prefill_chunk4096_ctx262144_sampled():
@@ -227,12 +260,15 @@ def test_encoder_prefill_chunk4096_ctx262144_sampled():
     for qi in (0, 1, 2047, Q - 2, Q - 1):
         ref_idx, ref_s = oracle.full_topk(u8(qI)[qi], w.numpy()[qi], kb, int(n_vis[qi]), k)
         check_topk(gi[qi], ref_idx, ref_s, np.arange(int(n_vis[qi])), k)
-        if not np.array_equal(gi[qi], ref_idx):
-            continue
+        same = np.array_equal(gi[qi], ref_idx)
         rows = oracle.prefill_swa_rows(pos[qi], W) - (p0 - W + 1)
         sel = np.where(ref_idx >= 0, ref_idx % R, -1)
         for l in (0, L - 1):
             ref = oracle.sparse_attention(bits16(qs[l])[qi], c, s, sel, bits16(swas[l])[rows], len(rows))
-            check_attn(outs[l][qi:qi + 1], ref[None])
-            compared += 1
-    assert compared >= 6, "too few sampled queries had the oracle's exact Top-K"
+            if same:
+                got = outs[l][qi:qi + 1]
+            else:                         # tie-band difference: attend over the oracle's entries
+                got = attn_with_oracle_idx(qs[l][qi], codes[0], scales[0], ref_idx, swas[l][rows], W)
+            check_attn(got, ref[None])
+            compared += int(same)
+    assert compared >= 6, "too few sampled queries kept the group's own selection"
