@@ -54,6 +54,12 @@ int scan_init_attributes();
 int attn_tc_init_attributes();
 int launch_prefill_index(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys, float* scores,
                          int64_t stride, int32_t* st, cudaStream_t s);
+size_t prefill_select_ws_bytes(int Q, int64_t n_keys);
+int launch_prefill_candidates(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys,
+                              const int64_t* n_vis, void* tk, void* sel_ws, int32_t* st, cudaStream_t s);
+int launch_prefill_finish(const uint8_t* qI, const float* w, int Q, const uint8_t* kI, int64_t n_keys,
+                          const int64_t* n_vis, int k, int32_t* idx, float* scores, void* tk, void* sel_ws,
+                          int32_t* st, cudaStream_t s);
 size_t attn_ws_bytes(int64_t units, int H, int k, int W);
 size_t attn_group_ws_bytes(int64_t B, int H, int k, int W);
 int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
@@ -251,9 +257,11 @@ size_t csa2_workspace_size(int32_t op, int32_t B, int64_t n_max, int32_t k, int3
     case CSA2_OP_FORM_POOL: return ws_form_pool(B, n_max);
     case CSA2_OP_SPARSE_ATTN: return attn_ws_bytes(B, H, k, 128);
     case CSA2_OP_PREFILL_GROUP: {
-      // B = queries, n_max = entries: scores + Top-K + attention partials
+      // B = queries, n_max = entries: full score rows (written only for the
+      // query tiles whose candidates cannot serve them) + Top-K + attention
+      // partials + the sampled scores, thresholds and tile marks
       size_t m = align256((size_t)B * (size_t)n_max * 4) + topk_ws_bytes(B);
-      return m + attn_group_ws_bytes(B, H, k, 128);
+      return m + align256(attn_group_ws_bytes(B, H, k, 128)) + prefill_select_ws_bytes(B, n_max);
     }
     case CSA2_OP_FORM_POOL_BLOCK_MAX: return pool_block_max_ws_bytes(B, n_max);
     case CSA2_OP_LAYER_GROUP: {
@@ -553,7 +561,8 @@ int csa2_prefill_index_scores(const uint8_t* qI, const float* w, int32_t Q, int3
                               const uint8_t* kI, int64_t n_keys, float* scores, int64_t scores_stride,
                               int32_t* d_status, void* stream) {
   if (Q < 0 || n_keys < 0 || scores_stride < n_keys) return CSA2_ERR_INVALID_ARG;
-  if (H_I != 8 || d_I != 128 || n_keys > 0x7FFFFFFF || (int64_t)Q * 8 > 0x7FFFFFFF) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (H_I != 8 || d_I != 128 || n_keys > kMaxPrefillKeys || (int64_t)Q * 8 > 0x7FFFFFFF)
+    return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (Q == 0 || n_keys == 0) return CSA2_OK;
   if (!qI || !w || !kI || !scores || !aligned16(qI) || !aligned16(kI)) return CSA2_ERR_INVALID_ARG;
   int rc = ensure_init();
@@ -567,7 +576,8 @@ int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
   if (a->Q < 0 || a->n_reuse < 0 || a->n_keys < 0 || !a->q_layers || !a->swa_layers || !a->out_layers)
     return CSA2_ERR_INVALID_ARG;
   if (a->H_I != 8 || a->d_I != 128 || a->d != 512 || !topk_k_ok(a->k) || a->W < 0 || a->W > 128 ||
-      (a->H != 16 && a->H != 32 && a->H != 48 && a->H != 64) || a->n_keys > 0x7FFFFFFF)
+      (a->H != 16 && a->H != 32 && a->H != 48 && a->H != 64) || a->n_keys > kMaxPrefillKeys ||
+      (int64_t)a->Q * 8 > 0x7FFFFFFF)
     return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (a->Q == 0) return CSA2_OK;
   if (!a->n_vis || !a->codes || !a->scales || !a->kI || !a->qI || !a->w || !a->idx || !a->swa_len)
@@ -583,12 +593,16 @@ int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
   float* scores = static_cast<float*>(a->ws);
   void* tk = static_cast<char*>(a->ws) + align256((size_t)a->Q * (size_t)a->n_keys * 4);
   void* aws = static_cast<char*>(tk) + topk_ws_bytes(a->Q);
-  // events: [0] before the indexer GEMM, [1] after it, [2] after Top-K, [3 + l] after layer l
+  void* sel = static_cast<char*>(aws) + align256(attn_group_ws_bytes(a->Q, a->H, a->k, 128));
+  // events: [0] before the indexer GEMM, [1] after it (the sampled pass, the
+  // thresholds and the candidate-emitting pass), [2] after Top-K, [3 + l] after layer l
   if ((rc = rec(ev(0), s)) != CSA2_OK) return rc;
-  if ((rc = launch_prefill_index(a->qI, a->w, a->Q, a->kI, a->n_keys, scores, a->n_keys, a->d_status, s)) != CSA2_OK)
+  if ((rc = launch_prefill_candidates(a->qI, a->w, a->Q, a->kI, a->n_keys, a->n_vis, tk, sel, a->d_status, s)) !=
+      CSA2_OK)
     return rc;
   if ((rc = rec(ev(1), s)) != CSA2_OK) return rc;
-  if ((rc = launch_topk(scores, nullptr, a->n_keys, a->n_vis, 1, a->Q, a->n_keys, a->k, a->idx, tk, false, s)) != CSA2_OK)
+  if ((rc = launch_prefill_finish(a->qI, a->w, a->Q, a->kI, a->n_keys, a->n_vis, a->k, a->idx, scores, tk, sel,
+                                  a->d_status, s)) != CSA2_OK)
     return rc;
   if ((rc = rec(ev(2), s)) != CSA2_OK) return rc;
   const int n_layers = a->n_reuse + 1;

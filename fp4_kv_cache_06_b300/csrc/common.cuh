@@ -31,6 +31,8 @@ constexpr int kHistBins = 4096;        // level-0 Top-K histogram (12 key bits)
 constexpr int kCandCap = 8192;         // Top-K candidate buffer per row
 constexpr int kMaxTopK = 2048;
 constexpr int kBlock = 8;              // positions per pool block
+// Prefill entries: an entry index plus a tile's 127 lanes stays below 2^31.
+constexpr int64_t kMaxPrefillKeys = 0x7FFFFFFFll - 128;
 
 // ---- host bookkeeping ------------------------------------------------------
 void count_launch();

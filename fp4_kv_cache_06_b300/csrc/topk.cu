@@ -66,6 +66,7 @@ static TopkWs topk_ws(void* ws, int B) {
 }
 uint32_t* topk_ws_hist(void* ws) { return static_cast<uint32_t*>(ws); }
 TopkHdr* topk_ws_hdr(void* ws, int B) { return topk_ws(ws, B).hdr; }
+uint64_t* topk_ws_cand(void* ws, int B) { return topk_ws(ws, B).cand; }
 
 
 // Candidates of row b: the first ceil(n[b] / len_div) entries, at most n_max

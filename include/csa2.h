@@ -429,7 +429,7 @@ CSA2_API int csa2_layer_group(const csa2_group_args* args, void* stream);
  * Top-K each query's visible count.
  *   qI [Q][8][128] u8; w [Q][8] fp32; kI [n_keys][128] u8
  *   scores [Q][scores_stride] fp32, scores_stride >= n_keys
- * Supported: H_I = 8, d_I = 128. */
+ * Supported: H_I = 8, d_I = 128, n_keys <= 2^31 - 129, Q * 8 < 2^31. */
 CSA2_API int csa2_prefill_index_scores(const uint8_t* qI, const float* w,
                                        int32_t Q, int32_t H_I, int32_t d_I,
                                        const uint8_t* kI, int64_t n_keys,
@@ -462,16 +462,29 @@ typedef struct csa2_prefill_args {
   size_t ws_bytes;
   int32_t* d_status;     /* optional                                           */
   void* const* events;   /* optional HOST array of cudaEvent_t: [0] before the
-                            indexer GEMM, [1] after it, [2] after Top-K,
-                            [3 + l] after layer l's attention (recorded
-                            together for the up to 8 layers of one launch)   */
+                            indexer GEMM, [1] after it (its sampled pass,
+                            the thresholds and the candidate-emitting pass),
+                            [2] after Top-K, [3 + l] after layer l's
+                            attention (recorded together for the up to 8
+                            layers of one launch)                            */
   int32_t n_events;
 } csa2_prefill_args;
 
-/* One encoder group over a prefill chunk: the Full layer's indexer GEMM
- * (csa2_prefill_index_scores), Top-k of each query over its visible entries,
- * then sparse attention of the Full layer and of each Reuse layer with those
- * indices, every layer with its own Q and SWA rows. */
+/* One encoder group over a prefill chunk: Top-k of each query over its
+ * visible entries by the indexer score of csa2_prefill_index_scores, then
+ * sparse attention of the Full layer and of each Reuse layer with those
+ * indices, every layer with its own Q and SWA rows.
+ * The selection is fused into the tcgen05 indexer GEMM, and no score matrix
+ * is written in the usual case: a GEMM pass over every 16th (or sparser)
+ * entry tile gives each query a threshold (the r-th best sampled score, r
+ * sized for about 2048 entries at or above it; every visible entry when a
+ * query sees at most 8192), the full GEMM pass then emits only the entries
+ * at or above it, and the exact Top-k is taken over those. A query with
+ * fewer than min(k, visible) of them, or more than 8192, is selected from
+ * its full score row instead, which the GEMM then writes for its tile of 32
+ * queries. Entry tiles that no query of a tile can see are skipped. The
+ * result is the same Top-k in every case (score descending, then position
+ * ascending). Supported: n_keys <= 2^31 - 129. */
 CSA2_API int csa2_prefill_group(const csa2_prefill_args* args, void* stream);
 
 #ifdef __cplusplus

@@ -83,3 +83,132 @@ def test_prefill_group_causal(p0, Q, n_keys):
     # every query and layer was compared, and most through the group's own output
     assert compared["group"] + compared["oracle_idx"] == Q * L
     assert compared["group"] >= Q * L // 2, compared
+
+
+def _e4m3_bytes(x: torch.Tensor) -> torch.Tensor:
+    """float tensor -> E4M3 bytes (torch's own conversion)."""
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _e4m3_float(b: torch.Tensor) -> torch.Tensor:
+    return b.view(torch.float8_e4m3fn).to(torch.float32)
+
+
+def _prefill_topk(qI, w, kI, n_vis, k=512, H=64, W=128, seed=5):
+    """One Full-layer prefill group over the given indexer inputs; returns the
+    GPU Top-K [Q][k] (the attention runs too, on small random rows)."""
+    Q, n = qI.shape[0], kI.shape[0]
+    kv = synth.normal_bf16((n, 512), seed=seed, stream="kv").to(DEV)
+    codes = torch.empty((n, 256), dtype=torch.uint8, device=DEV)
+    scales = torch.empty((n, 32), dtype=torch.uint8, device=DEV)
+    csa2.csa2_quantize_kv_fp4(kv[None], codes[None], scales[None])
+    qs = [synth.normal_bf16((Q, H, 512), seed=seed, stream="q").to(DEV)]
+    swas = [synth.normal_bf16((Q + W - 1, 512), seed=seed, stream="swa").to(DEV)]
+    outs = [torch.empty((Q, H, 512), dtype=torch.bfloat16, device=DEV)]
+    idx = torch.empty((Q, k), dtype=torch.int32, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_PREFILL_GROUP, Q, n, k, 0, H))
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    swa_len = torch.full((Q,), W, dtype=torch.int32, device=DEV)
+    csa2.csa2_prefill_group(torch.as_tensor(n_vis, dtype=torch.int64).to(DEV), codes, scales, kI.to(DEV),
+                            qI.to(DEV), w.to(DEV), idx, qs, swas, swa_len, outs, ws, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return idx.cpu().numpy()
+
+
+def test_prefill_selection_sampled_thresholds():
+    """Rows longer than the candidate list (8192): the selection takes its
+    per-query thresholds from the sampled pass. Visible counts vary from 9000
+    to 20000, and a few queries see at most 8192 entries (every entry is
+    then a candidate)."""
+    Q, n = 64, 20000
+    qI = synth.normal_e4m3((Q, 8, 128), seed=61, stream="qI")
+    w = synth.uniform_f32((Q, 8), seed=61, stream="w")
+    kI = synth.indexer_keys_e4m3((n, 128), seed=61, bias_prob=0.05)
+    n_vis = np.linspace(9000, n, Q).astype(np.int64)
+    n_vis[[3, 17]] = [8192, 5000]
+    gi = _prefill_topk(qI, w, kI, n_vis)
+    for q in range(Q):
+        ref_idx, ref_s = oracle.full_topk(u8(qI)[q], w.numpy()[q], u8(kI), int(n_vis[q]), 512)
+        check_topk(gi[q], ref_idx, ref_s, np.arange(int(n_vis[q])), 512)
+
+
+def test_prefill_selection_all_scores_equal():
+    """Every score equal (zero indexer keys): every visible entry ties at the
+    threshold, the candidate list overflows, and the query tile's rows are
+    scored in full and selected there. Ties go to the smallest positions."""
+    Q, n = 40, 12000
+    qI = synth.normal_e4m3((Q, 8, 128), seed=62, stream="qI")
+    w = synth.uniform_f32((Q, 8), seed=62, stream="w")
+    kI = torch.zeros((n, 128), dtype=torch.uint8)
+    n_vis = np.full(Q, n, dtype=np.int64)
+    n_vis[5] = 300                                   # fewer than k visible: all of them, then -1
+    gi = _prefill_topk(qI, w, kI, n_vis)
+    for q in range(Q):
+        m = min(512, int(n_vis[q]))
+        expect = np.full(512, -1, dtype=np.int32)
+        expect[:m] = np.arange(m)
+        assert np.array_equal(gi[q], expect), q
+
+
+def test_prefill_selection_too_few_candidates():
+    """High scores only inside the sampled entry tiles (300 entries of tiles
+    0, 16, 32, 48, 64): the sampled threshold then lies among them and fewer
+    than k entries reach it, so the rows are scored in full and selected
+    there. The result is still the oracle's Top-512."""
+    Q, n = 32, 9000
+    qf = _e4m3_float(synth.normal_e4m3((Q, 8, 128), seed=63, stream="qI")).abs()
+    qI = _e4m3_bytes(qf)
+    w = synth.uniform_f32((Q, 8), seed=63, stream="w")
+    kI = synth.indexer_keys_e4m3((n, 128), seed=63)
+    hi = _e4m3_float(synth.normal_e4m3((300, 128), seed=63, stream="kv_new")).abs() * 4
+    rows = np.concatenate([np.arange(60) + t * 16 * 128 for t in range(5)])
+    kI[torch.from_numpy(rows)] = _e4m3_bytes(hi)
+    n_vis = np.full(Q, n, dtype=np.int64)
+    gi = _prefill_topk(qI, w, kI, n_vis)
+    for q in range(Q):
+        ref_idx, ref_s = oracle.full_topk(u8(qI)[q], w.numpy()[q], u8(kI), n, 512)
+        assert set(rows.tolist()) <= set(ref_idx.tolist())       # the construction holds
+        check_topk(gi[q], ref_idx, ref_s, np.arange(n), 512)
+
+
+def test_prefill_index_scores_beyond_one_launch():
+    """More than 2048 query tiles (65,600 queries): the scores come from
+    several launches of the persistent kernel; sampled rows of each match
+    the oracle."""
+    Q, n = 65600, 256
+    qI = synth.normal_e4m3((Q, 8, 128), seed=64, stream="qI")
+    w = synth.uniform_f32((Q, 8), seed=64, stream="w")
+    kI = synth.indexer_keys_e4m3((n, 128), seed=64)
+    scores = torch.empty((Q, n), dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    csa2.csa2_prefill_index_scores(qI.to(DEV), w.to(DEV), kI.to(DEV), scores, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    s = scores.cpu().numpy()
+    for q in (0, 31, 32, 65535, 65536, 65599):
+        ref = oracle.indexer_scores(u8(qI)[q], w.numpy()[q], u8(kI))
+        np.testing.assert_allclose(s[q], ref, rtol=2e-6, atol=1e-6)
+
+
+def test_prefill_selection_ties_split_by_position():
+    """Every indexer key row appears twice (rows j and j + 2000), so scores tie
+    in pairs and the 512th place falls on a tie: among equal scores the
+    smaller positions are taken. Up to 8192 visible entries are all
+    candidates, so this exercises the candidate list's tie split; the result
+    must equal the oracle's exactly."""
+    Q, half = 40, 2000
+    qI = synth.normal_e4m3((Q, 8, 128), seed=65, stream="qI")
+    w = synth.uniform_f32((Q, 8), seed=65, stream="w")
+    base = synth.indexer_keys_e4m3((half, 128), seed=65)
+    kI = torch.cat([base, base], 0)
+    n_vis = np.full(Q, 2 * half, dtype=np.int64)
+    n_vis[7] = 1500                                  # part of the pairs visible
+    gi = _prefill_topk(qI, w, kI, n_vis)
+    ties = 0
+    for q in range(Q):
+        ref_idx, ref_s = oracle.full_topk(u8(qI)[q], w.numpy()[q], u8(kI), int(n_vis[q]), 512)
+        assert np.array_equal(gi[q], ref_idx), q
+        kth = np.sort(ref_s)[::-1][511]
+        ties += int(np.count_nonzero(ref_s == kth) > 1)
+    assert ties > Q // 2                             # the construction puts ties at the boundary
