@@ -42,7 +42,7 @@
 //   1. sampled pass (write mode): the scores of every S-th entry tile
 //      (S >= 16, at most 16 sampled tiles: 2048 entries);
 //   2. threshold: per query, the score key of the r-th best visible sampled
-//      score, r chosen so that about 2560 visible entries are expected at or
+//      score, r chosen so that about 2048 visible entries are expected at or
 //      above it (a warp bisection over register-held keys). A query with at
 //      most kCandCap visible entries takes all of them (threshold key 0);
 //   3. filter pass over every visible unit;
@@ -54,7 +54,7 @@
 //      register-held score keys, the radix select when a tie at the boundary
 //      score must be split by position), and over each marked query's full
 //      row (a warp; radix select).
-// In the common case nothing but ~2560 candidates per query is written.
+// In the common case nothing but ~2048 candidates per query is written.
 //
 // Every wait is bounded; a timeout writes CSA2_ERR_TIMEOUT to d_status and
 // the CTA winds down (waiting, again bounded, for its own MMAs) before
@@ -80,7 +80,7 @@ constexpr uint32_t kPQBytes = kPN * kPK;          // 32 KB
 constexpr int kPMaxQTiles = 2048;                 // query tiles per launch (the unit table)
 constexpr int kPSampleMin = 16;                   // sampled pass: every S-th entry tile, S >= 16,
 constexpr int kPSampleTiles = 16;                 //   at most 16 sampled tiles (2048 entries)
-constexpr int kPCandTarget = 2560;                // candidates expected per query
+constexpr int kPCandTarget = 2048;                // candidates expected per query
 constexpr int kPChunk = 32;                       // candidate-list slots reserved per warp and query at a time
 constexpr int kPSelWarps = 4;                     // selection kernels: one warp per query (32 KB)
 constexpr int kPSelBins = 2048;                   // radix digits of 11 bits (a warp's histogram)
@@ -135,7 +135,7 @@ struct UnitWalk {
   const int64_t* pre;
   int qtiles;
   int qi;
-  int64_t t;
+  int t, vt;                 // sequence tile within query tile qi, and qi's unit count (< 2^24)
   __device__ void start(int64_t u) {
     int lo = 0, hi = qtiles - 1;                 // last qi with pre[qi] <= u
     while (lo < hi) {
@@ -143,13 +143,15 @@ struct UnitWalk {
       if (pre[mid] <= u) lo = mid; else hi = mid - 1;
     }
     qi = lo;
-    t = u - pre[qi];
+    t = (int)(u - pre[qi]);
+    vt = (int)(pre[qi + 1] - pre[qi]);
   }
-  __device__ bool last_of_tile() const { return t + 1 >= pre[qi + 1] - pre[qi]; }
+  __device__ bool last_of_tile() const { return t + 1 >= vt; }
   __device__ void next() {
-    if (last_of_tile()) {
+    if (t + 1 >= vt) {
       do { ++qi; } while (qi < qtiles && pre[qi + 1] == pre[qi]);
       t = 0;
+      if (qi < qtiles) vt = (int)(pre[qi + 1] - pre[qi]);
     } else {
       ++t;
     }
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(const __grid_con
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sp + L::kTmemSlot);
-  UnitWalk it{sPre, a.qtiles, 0, 0};
+  UnitWalk it{sPre, a.qtiles, 0, 0, 0};
   it.start(u0);
 
   if (warp == 0 && lane == 0) {
@@ -320,7 +322,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(const __grid_con
       // never loaded nor signalled, so the MMA issuer's wait on it runs out
       if (a.fault && i == 1) break;
       tc::mbar_expect_tx(bar_full + 8 * s, kPTileBytes);
-      tc::tma_load_2d(base + L::kA + s * kPTileBytes, &map_k, 0, (int)(it.t * span), bar_full + 8 * s);
+      tc::tma_load_2d(base + L::kA + s * kPTileBytes, &map_k, 0, it.t * (int)span, bar_full + 8 * s);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -372,7 +374,10 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(const __grid_con
     uint32_t cur[kPQw], pre[kPQw];
 #pragma unroll
     for (int qq = 0; qq < kPQw; ++qq) { cur[qq] = 0; pre[qq] = 0; }
-    int64_t minvis = 0;                         // filter: fewest visible entries of the warp's queries
+    int32_t minvis = 0;                         // filter: fewest visible entries of the warp's queries
+    float* rowp = a.scores;                     // write: row of the warp's first query
+    uint32_t rows_ok = 0;                       // write: bit qq set when query q0 + qq exists
+    const int32_t span32 = (int32_t)span, nk32 = (int32_t)a.n_keys;   // both < 2^31
     int qi_prev = -1, q0_prev = 0;
     bool aborted = false;
     // filter: mark the holes of the warp's queries q0 .. (at the end of their tile)
@@ -415,29 +420,39 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(const __grid_con
             const int64_t o = __shfl_xor_sync(0xffffffffu, mv, off);
             mv = o < mv ? o : mv;
           }
-          minvis = mv;
+          minvis = (int32_t)mv;
 #pragma unroll
           for (int qq = 0; qq < kPQw; ++qq) {
             cur[qq] = __shfl_sync(0xffffffffu, base, qq);
             pre[qq] = cur[qq] + kPChunk;
           }
         }
+        if (kMode == kPWrite) {
+          rowp = a.scores + (int64_t)q0 * a.stride;
+          rows_ok = 0;
+#pragma unroll
+          for (int qq = 0; qq < kPQw; ++qq) rows_ok |= (q0 + qq < a.Q ? 1u : 0u) << qq;
+        }
         __syncwarp();
         qi_prev = it.qi;
         q0_prev = q0;
       }
       const int acc = i & 1;
-      // warp-uniform decision: the TMEM loads below are warp-collective
-      const bool got = tc::mbar_wait(bar_tfull + 8 * acc, (i >> 1) & 1, a.wait_ns);
-      if (!__all_sync(0xffffffffu, got) || __any_sync(0xffffffffu, *s_abort != 0)) {
+      // warp-uniform decision: the TMEM loads below are warp-collective. A
+      // role that stopped (timeout) stops the commits, so this wait then runs
+      // out as well; no separate abort check is needed on the way.
+      const uint32_t tf_bar = bar_tfull + 8 * acc, tf_par = (i >> 1) & 1;
+      const bool got = tc::mbar_try_wait(tf_bar, tf_par) || tc::mbar_wait(tf_bar, tf_par, a.wait_ns);
+      if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) { report(a.st, CSA2_ERR_TIMEOUT); *s_abort = 1; }
         aborted = true;
         break;
       }
       tc::tc_fence_after();
-      const int32_t entry = (int32_t)(it.t * span) + sub * 32 + lane;   // < n_keys + 128 <= 2^31 - 1
-      const int64_t col = it.t * kPM + sub * 32 + lane;
-      const bool fullvis = it.t * span + kPM <= minvis;                  // filter: no entry past any limit
+      const int32_t tb = it.t * span32;                                  // the tile's first entry
+      const int32_t entry = tb + sub * 32 + lane;                        // < n_keys + 128 <= 2^31 - 1
+      const int32_t col = it.t * kPM + sub * 32 + lane;
+      const bool fullvis = tb + kPM <= minvis;                           // filter: no entry past any limit
       const uint32_t taddr = tmem + ((uint32_t)(sub * 32) << 16) + acc * kPN + grp * (kPQw * kPH);
       // four 16-column chunks (2 queries each): chunk c + 1 is read from TMEM
       // while chunk c is summed; the accumulator is handed back once the last
@@ -471,11 +486,11 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_index(const __grid_con
       }
       {
         if (kMode == kPWrite) {
+          float* pc = rowp + col;
+          const bool inside = tb + kPM <= nk32 || entry < nk32;
 #pragma unroll
-          for (int qq8 = 0; qq8 < 8; ++qq8) {
-            const int q = q0 + qq8;
-            if (q < a.Q && entry < a.n_keys) a.scores[(int64_t)q * a.stride + col] = scv[qq8];
-          }
+          for (int qq8 = 0; qq8 < 8; ++qq8)
+            if (((rows_ok >> qq8) & 1u) && inside) pc[(int64_t)qq8 * a.stride] = scv[qq8];
         } else {
           const float4 ta = reinterpret_cast<const float4*>(sTau)[0];
           const float4 tb = reinterpret_cast<const float4*>(sTau)[1];
