@@ -829,7 +829,7 @@ def run_prefill(args, world, rank, local):
                    "first_query_token": wl.p0, "heads": cfg.H, "indexer": f"{cfg.H_I}x{cfg.d_I}",
                    "topk": cfg.k, "swa": cfg.W, "layers": wl.layers, "groups": [list(g) for g in cfg.groups],
                    "separate_group_caches": cfg.group_caches, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (2 GiB score matrix per step)"},
+                   "l2": "inputs larger than L2: every layer's queries, Q x 64 x 512 bf16 (268 MB at 4096 queries)"},
         "roofline": {"bound": "tensor", "kernel": "k_prefill_index (tcgen05 FP8 indexer GEMM)",
                      "achieved": round(ach, 1), "peak": fp8_peak, "peak_kind": kind, "unit": "TFLOP/s",
                      "frac": round(ach / fp8_peak, 4), "traffic": None, "gemm_ms": round(gemm_ms, 4),
