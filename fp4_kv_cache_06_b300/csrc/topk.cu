@@ -378,16 +378,22 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
 // above d (both 0 for an inconsistent histogram).
 __device__ void warp_digit_from_top(const uint32_t* h, uint32_t need, int* digit, uint32_t* above) {
   const int lane = threadIdx.x & 31;
-  uint32_t sum = 0;
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) sum += h[1023 - 32 * lane - ((i + lane) & 31)];
-  uint32_t incl = sum;
+  // row j (from the top) holds digits 1023 - 32 j - i, i = 0..31; lane l
+  // reads element l of every row (consecutive words: conflict-free), the 32
+  // loads independent, and each row's total is one warp reduction
+  uint32_t row_tot = 0;                                // lane j: the total of row j
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t t = __reduce_add_sync(0xffffffffu, h[1023 - 32 * j - lane]);
+    if (lane == j) row_tot = t;
+  }
+  uint32_t incl = row_tot;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const uint32_t t = __shfl_up_sync(0xffffffffu, incl, off);
     if (lane >= off) incl += t;
   }
-  const uint32_t excl = incl - sum;
+  const uint32_t excl = incl - row_tot;
   const uint32_t hit = __ballot_sync(0xffffffffu, excl < need && incl >= need);
   *digit = 0;
   *above = 0;
@@ -511,7 +517,14 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
   const int64_t nb = row_len(n, b, len_div, n_max);
   const float* s = scores + (int64_t)b * stride;
   const int32_t* cp = cand_pos ? cand_pos + (int64_t)b * stride : nullptr;
-  if (hdr[b].overflow) {
+  // the row header in one 16-byte load: {cnt, overflow, done, vbin}
+  const uint4 hv = *reinterpret_cast<const uint4*>(hdr + b);
+  // direct mode: the first eight entries of this thread, loaded before the
+  // header is looked at (harmless reads of the row on the other paths)
+  float v[8];
+  int32_t p[8];
+  if (mode == kFinDirect) load8(s, cp, (int64_t)tid * 8, nb, v, p);
+  if (hv.y) {
     // slow path: count the row's present candidates, then select over global memory
     __shared__ uint32_t s_valid;
     if (tid == 0) s_valid = 0;
@@ -524,16 +537,17 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
     select_and_write(src, k, (int64_t)s_valid, out, h, sel);
     return;
   }
-  const int vbin = hdr[b].vbin;
+  const int vbin = (int)hv.w;
   int cnt = 0;
   if (mode == kFinDirect) {
-    // the row itself, in index order: entries at or above the threshold bin
+    // the row itself, in index order: entries at or above the threshold bin;
+    // the next 8192 entries load while these are compacted
     uint32_t run = 0;
     for (int64_t i0 = 0; i0 < nb; i0 += (int64_t)kFinThreads * 8) {
-      const int64_t i = i0 + (int64_t)tid * 8;
-      float v[8];
-      int32_t p[8];
-      load8(s, cp, i, nb, v, p);
+      float vn[8];
+      int32_t pn[8];
+      const int64_t nxt = i0 + (int64_t)kFinThreads * 8;
+      if (nxt < nb) load8(s, cp, nxt + (int64_t)tid * 8, nb, vn, pn);
       uint32_t take = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
@@ -547,6 +561,10 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
         ++slot;
       }
       run += tot;
+      if (nxt < nb) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) { v[u] = vn[u]; p[u] = pn[u]; }
+      }
     }
     cnt = (int)min(run, (uint32_t)kCandCap);
   } else if (mode == kFinTable) {
@@ -595,7 +613,7 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
       if (o < cnt) keys[o] = kv[u];
     }
   } else {
-    cnt = (int)min(hdr[b].cnt, (uint32_t)kCandCap);
+    cnt = (int)min(hv.x, (uint32_t)kCandCap);
     for (int i = tid; i < cnt; i += kFinThreads) keys[i] = cand[(int64_t)b * kCandCap + i];
   }
   __syncthreads();
