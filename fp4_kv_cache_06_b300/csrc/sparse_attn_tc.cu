@@ -27,11 +27,12 @@
 //             (rows reaching 2^23 are reported as out of range). Below 2^-14
 //             a value keeps an absolute accuracy of 2^-25; absent rows are
 //             zero;
-//   MMA (warp 12, one thread): S(t) = Q K(t)^T with tcgen05.mma kind::f16,
-//             M = 64 heads, N = 64 keys, K = 512, into one
-//             of two S buffers in TMEM, and O += P(t) V(t); each is issued as
-//             soon as its inputs are ready, so S(t+1) overlaps the softmax of
-//             tile t;
+//   MMA (one thread each of warps 12 and 13): warp 12 issues
+//             S(t) = Q K(t)^T with tcgen05.mma kind::f16, M = 64 heads,
+//             N = 64 keys, K = 512, into one of two S buffers in TMEM, as
+//             soon as tile t is ready and the softmax has read S(t - 2);
+//             warp 13 issues O += P(t) V(t) as soon as P(t) is ready, so PV
+//             never waits behind the issue of an S;
 //   softmax (warps 0-3, two threads per head: key columns 0..31 and
 //             32..63): reads S, takes the tile's per-head maximum across the
 //             two halves by a shuffle, raises the running max only when a
@@ -59,14 +60,15 @@ namespace csa2 {
 
 constexpr int kTD = 512;                  // head dim
 constexpr int kTT = 64;                   // keys per tile
-constexpr int kTThreads = 416;            // warps 0-3 softmax/correction, 4-11 producers, 12 MMA
+constexpr int kTThreads = 448;            // warps 0-3 softmax/correction, 4-11 producers, 12 S issue, 13 PV issue
 constexpr int kSoftWarps = 4;
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kProdBase = kSoftThreads;   // first producer thread
 constexpr int kProd = 256;                // producer threads
 constexpr int kProdWarps = kProd / 32;
 constexpr int kItems = kTT / kProdWarps;  // FP4 rows per producer thread and tile (one 16-channel group each)
-constexpr int kMmaWarp = 12;
+constexpr int kMmaWarp = 12;             // issues S; allocates TMEM
+constexpr int kPvWarp = 13;              // issues PV
 constexpr int kRing = 8;                  // row-source ring: tiles j-2 .. j+3 may be live at once
 constexpr uint32_t kTOcol = 256;
 
@@ -98,7 +100,9 @@ constexpr int kBarPFull = 6;              // P ready (one arrive after the softm
 constexpr int kBarODone = 7;              // PV done (tcgen05.commit)
 constexpr int kBarFin = 8;                // every MMA of the CTA done (tcgen05.commit)
 constexpr int kBarQ = 9;                  // Q converted (every thread of the converting warps arrives)
-constexpr int kQWarps = kSoftWarps + 1;   // the softmax warps and the MMA warp convert Q
+constexpr int kBarSFree = 10;             // [2] S buffer read by the softmax (the PV warp arrives)
+constexpr int kBarSFin = 12;              // every S MMA done (tcgen05.commit of the S warp)
+constexpr int kQWarps = kSoftWarps + 2;   // the softmax warps and the two MMA warps convert Q
 
 __device__ __forceinline__ uint32_t kt_off(int row, int chunk) {     // chunk = 16-byte unit of 8 dims
   return (uint32_t)((chunk >> 3) * 8192 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
@@ -230,6 +234,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     tc::mbar_init(bar(kBarODone), 1);
     tc::mbar_init(bar(kBarFin), 1);
     tc::mbar_init(bar(kBarQ), 32 * kQWarps);
+    tc::mbar_init(bar(kBarSFree), 1);
+    tc::mbar_init(bar(kBarSFree + 1), 1);
+    tc::mbar_init(bar(kBarSFin), 1);
     tc::fence_barrier_init();
     sMisc[1] = 0;
     sMisc[2] = 0;
@@ -299,12 +306,12 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   pdl_trigger();                              // TMEM is held: the next kernel may start launching
   // Q -> fp16, one warp per head: scaled by 2^-a so that the head's largest
   // magnitude lies in [2^14, 2^15) (heads >= H and all-zero heads: a = 0).
-  // The softmax warps and the MMA warp do this while the producers start on
-  // tile 0; tile 1 goes into key buffer 1 (the bf16 staging of Q) only after
+  // The softmax warps and the two MMA warps do this while the producers
+  // start on tile 0; tile 1 goes into key buffer 1 (the bf16 staging of Q) only after
   // every converting warp has arrived on kBarQ, and S and the softmax wait
   // for it too.
-  if (warp < kSoftWarps || warp == kMmaWarp) {
-    for (int h = warp < kSoftWarps ? warp : kSoftWarps; h < 64; h += kQWarps) {
+  if (warp < kSoftWarps || warp >= kMmaWarp) {
+    for (int h = warp < kSoftWarps ? warp : kSoftWarps + (warp - kMmaWarp); h < 64; h += kQWarps) {
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
       if (h < H) {
         v0 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane));
@@ -561,7 +568,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     }
     l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
   } else {
-    // ================= MMA issue (one thread) =================
+    // ================= MMA issue (lane 0 of warps 12 and 13) =================
     if (lane == 0) {
       const uint32_t idesc_s = tc::instr_desc(tc::kFmtF16, tc::kFmtF16, 0, 0, 64, kTT);   // heads: M = 64
       const uint32_t idesc_o = tc::instr_desc(tc::kFmtF16, tc::kFmtF16, 0, 1, 128, 256);
@@ -590,40 +597,39 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         }
         tc::mma_commit(bar(kBarSFull + (j & 1)));
       };
-      // Issue S(js) once its key tile is ready (and S(js - 2)'s softmax has
-      // handed over, i.e. PV(js - 2) was issued), and PV(jp) once its P is
-      // ready; whichever comes first. The polls share one time bound.
-      bool ok = true;
-      if (!tc::mbar_wait(bar(kBarQ), 0, wait_ns)) ok = false;
-      int js = 0, jp = 0;
-      uint64_t t0 = tc::globaltimer_ns();
-      uint32_t polls = 0;
-      while (ok && jp < nt) {
-        bool progressed = false;
-        if (js < nt && js <= jp + 1 && tc::mbar_test_wait(bar(kBarKvFull + (js & 1)), (js >> 1) & 1)) {
+      // Two issuers: this warp issues S(js) as soon as its key tile is ready
+      // and the softmax has read S(js - 2) from the same TMEM buffer; the PV
+      // warp issues PV(jp) as soon as P(jp) is ready. PV no longer waits
+      // behind the issue of a 32-instruction S.
+      if (warp == kMmaWarp) {
+        bool ok = tc::mbar_wait(bar(kBarQ), 0, wait_ns);
+        for (int js = 0; ok && js < nt; ++js) {
+          ok = tc::mbar_wait(bar(kBarKvFull + (js & 1)), (js >> 1) & 1, wait_ns);
+          if (ok && js >= 2) ok = tc::mbar_wait(bar(kBarSFree + (js & 1)), ((js >> 1) - 1) & 1, wait_ns);
+          if (!ok || sMisc[3]) { ok = false; break; }
           tc::tc_fence_after();
-          issue_s(js++);
-          progressed = true;
+          issue_s(js);
         }
-        if (jp < js && tc::mbar_test_wait(bar(kBarPFull), jp & 1)) {
+        if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
+        // every S MMA has completed before TMEM is read or freed
+        tc::mma_commit(bar(kBarSFin));
+        if (!tc::mbar_wait(bar(kBarSFin), 0, wait_ns)) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
+      } else {
+        bool ok = true;
+        int jp = 0;
+        for (; jp < nt; ++jp) {
+          ok = tc::mbar_wait(bar(kBarPFull), jp & 1, wait_ns);
+          if (!ok || sMisc[3]) { ok = false; break; }
           tc::tc_fence_after();
-          issue_pv(jp++);
-          progressed = true;
+          tc::mbar_arrive(bar(kBarSFree + (jp & 1)));   // the softmax read S(jp) before P(jp) was ready
+          issue_pv(jp);
         }
-        if (progressed) {
-          t0 = tc::globaltimer_ns();
-          polls = 0;
-        } else if ((++polls & 255) == 0 && (sMisc[3] || tc::globaltimer_ns() - t0 > wait_ns)) {
-          ok = false;
-          break;
-        }
+        if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
+        // every PV MMA has completed before TMEM is read or freed
+        tc::mma_commit(bar(kBarFin));
+        if (!tc::mbar_wait(bar(kBarFin), 0, wait_ns)) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
+        if (jp < nt) sMisc[3] = 1;
       }
-      const int issued_pv = jp;
-      if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
-      // every MMA of this CTA has completed before TMEM is read or freed
-      tc::mma_commit(bar(kBarFin));
-      if (!tc::mbar_wait(bar(kBarFin), 0, wait_ns)) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
-      if (issued_pv < nt) sMisc[3] = 1;
     }
     __syncwarp();
   }
