@@ -10,9 +10,8 @@
 // [CED]  same page, section "Каузальный энкодер-декодер: вдвое меньший
 //        префилл": 128-token sliding window in every layer.
 //
-// Key slots are processed in tiles of 64 (the layer's SWA rows first, so
-// their bf16 copies overlap the set-up and the first tile; then the gathered
-// rows) by a warp-specialised pipeline:
+// Key slots are processed in tiles of 64 (the layer's SWA rows first, then
+// the gathered rows) by a warp-specialised pipeline:
 //   producers (warps 4-11): row sources from the Top-K indices three tiles
 //             ahead; the FP4 rows prefetched into registers two tiles ahead,
 //             then
@@ -20,8 +19,9 @@
 //             scale as a packed f16 multiply: the product, <= 6 significant
 //             bits in 2^-10 .. 2688, is exact in fp16) into one of two key
 //             buffers in the K-major 128-byte-swizzle layout
-//             [dim/64][key][128 B]. SWA rows (bf16) are copied in with
-//             cp.async and converted in place; a row whose largest magnitude
+//             [dim/64][key][128 B]. SWA rows (bf16) are loaded into
+//             registers, four rows per warp in flight, converted there and
+//             stored once; a row whose largest magnitude
 //             reaches 2^16 is first scaled by 2^-b (b <= 7, exact), and its
 //             logits and probabilities are scaled back by 2^b in the softmax
 //             (rows reaching 2^23 are reported as out of range). Below 2^-14
@@ -69,6 +69,7 @@ constexpr int kProdWarps = kProd / 32;
 constexpr int kItems = kTT / kProdWarps;  // FP4 rows per producer thread and tile (one 16-channel group each)
 constexpr int kMmaWarp = 12;             // issues S; allocates TMEM
 constexpr int kPvWarp = 13;              // issues PV
+static_assert(kPvWarp == kMmaWarp + 1 && kTThreads == 32 * (kPvWarp + 1), "warp roles: the last two warps issue MMAs");
 constexpr int kRing = 8;                  // row-source ring: tiles j-2 .. j+3 may be live at once
 constexpr uint32_t kTOcol = 256;
 
@@ -183,6 +184,12 @@ __device__ __forceinline__ uint2 ldg_hint_u2(const void* p, uint64_t pol) {
   asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
   return v;
 }
+__device__ __forceinline__ uint4 ldg_hint_u4(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+  return v;
+}
 __device__ __forceinline__ uint32_t ldg_hint_u8(const void* p, uint64_t pol) {
   uint16_t v;
   asm volatile("ld.global.nc.L2::cache_hint.u8 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
@@ -292,13 +299,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     for (int j = 0; j < 3 && j < nt; ++j) row_sources(j, tid);
   }
   __syncthreads();
-  // the SWA rows of tile 0 (bf16, converted by the producers) travel with Q
-  for (int e = tid; e < kTT * 64 && nt > 0; e += kTThreads) {
-    const int r = e >> 6, c = e & 63;
-    const int64_t s0 = sSrc[r];
-    if (s0 <= -2) cp_async16_hint(base + L::kKV + kt_off(r, c), swa + (-2 - s0) * kTD + c * 8, pol_stream);
-  }
-  cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
   tc::tc_fence_after();
@@ -361,7 +361,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     auto produce = [&](int j, uint2* cw, uint32_t* sb) -> bool {
       if (named_or(kNbProd, kProd, sMisc[3] != 0)) return false;
       const int buf = j & 1, slot = j % kRing;
-      const uint32_t kv = base + L::kKV + buf * L::kKVBytes;
       unsigned char* kvp = sp + L::kKV + buf * L::kKVBytes;
       // key buffer 1 held the bf16 Q until the converting warps were done
       if (j == 1 && !tc::mbar_wait(bar(kBarQ), 0, wait_ns)) {
@@ -377,19 +376,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       const uint64_t valid = (uint64_t)sMask[slot * 2] | ((uint64_t)sMask[slot * 2 + 1] << 32);
       const uint64_t fp4 = (uint64_t)sFp4[slot * 2] | ((uint64_t)sFp4[slot * 2 + 1] << 32);
       const uint64_t swa_rows = valid & ~fp4;
-      // absent rows: zero; SWA rows: bf16 straight into the key buffer (tile
-      // 0's came with Q). Warp pw takes rows pw + 8 m, a lane two 16-byte chunks.
-      if (~fp4 != 0) {
+      // absent rows: zero. Warp pw takes rows pw + 8 m, a lane two 16-byte chunks.
+      if (~valid != 0) {
         for (int r = pw; r < kTT; r += kProdWarps) {
-          if (!((valid >> r) & 1)) {
+          if (!((valid >> r) & 1))
             for (int c = lane; c < 64; c += 32) *reinterpret_cast<uint4*>(kvp + kt_off(r, c)) = make_uint4(0, 0, 0, 0);
-          } else if (j > 0 && ((swa_rows >> r) & 1)) {
-            const __nv_bfloat16* row = swa + (-2 - src[r]) * kTD;
-            for (int c = lane; c < 64; c += 32) cp_async16_hint(kv + kt_off(r, c), row + c * 8, pol_stream);
-          }
         }
       }
-      cp_async_commit();
       // FP4 rows of this tile (in registers): one 16-channel group per item
 #pragma unroll
       for (int i = 0; i < kItems; ++i) {
@@ -407,30 +400,43 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         *reinterpret_cast<uint4*>(kvp + kt_off(r, 2 * g)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(kvp + kt_off(r, 2 * g + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      // SWA rows: bf16 -> fp16 in place. Each thread converts the chunks it
-      // copied itself (tile 0's were copied and waited for during set-up).
-      // A row whose largest magnitude reaches 2^16 (beyond fp16) is scaled by
-      // 2^-b first (b = its binary exponent - 15, at most 7: rows reaching
-      // 2^23 saturate and are reported); b goes to the softmax through kKeyB.
+      // SWA rows: bf16 from global memory into registers (four rows of a warp
+      // in flight), converted there and stored once as fp16. A row whose
+      // largest magnitude reaches 2^16 (beyond fp16) is scaled by 2^-b first
+      // (b = its binary exponent - 15, at most 7: rows reaching 2^23
+      // saturate and are reported); b goes to the softmax through kKeyB.
       if (swa_rows) {
-        cp_async_wait<0>();
-        for (int r = pw; r < kTT; r += kProdWarps) {
-          if (!((swa_rows >> r) & 1)) continue;
-          uint4* p0 = reinterpret_cast<uint4*>(kvp + kt_off(r, lane));
-          uint4* p1 = reinterpret_cast<uint4*>(kvp + kt_off(r, lane + 32));
-          const uint4 v0 = *p0, v1 = *p1;
-          const int e = (int)(__reduce_max_sync(0xffffffffu, bf16x16_max_mag(v0, v1)) >> 7) - 127;
-          int bsh = e >= 16 ? e - 15 : 0;
-          if (bsh > 7) {
-            if (lane == 0) report(st, CSA2_ERR_DEVICE_RANGE);
-            bsh = 7;
+#pragma unroll 1
+        for (int r0 = pw; r0 < kTT; r0 += 4 * kProdWarps) {
+          uint4 va[4][2];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = r0 + u * kProdWarps;
+            va[u][0] = make_uint4(0, 0, 0, 0);
+            va[u][1] = va[u][0];
+            if (r < kTT && ((swa_rows >> r) & 1)) {
+              const __nv_bfloat16* row = swa + (-2 - src[r]) * kTD;
+              va[u][0] = ldg_hint_u4(row + lane * 8, pol_stream);
+              va[u][1] = ldg_hint_u4(row + (lane + 32) * 8, pol_stream);
+            }
           }
-          const float f = pow2f(-bsh);
-          *p0 = bf16x8_to_f16x8_scaled(v0, f);
-          *p1 = bf16x8_to_f16x8_scaled(v1, f);
-          if (bsh != 0 && lane == 0) {
-            sKeyB[slot * kTT + r] = (uint8_t)bsh;
-            sKeyFlag[slot] = 1;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = r0 + u * kProdWarps;
+            if (r >= kTT || !((swa_rows >> r) & 1)) continue;       // warp-uniform
+            const int e = (int)(__reduce_max_sync(0xffffffffu, bf16x16_max_mag(va[u][0], va[u][1])) >> 7) - 127;
+            int bsh = e >= 16 ? e - 15 : 0;
+            if (bsh > 7) {
+              if (lane == 0) report(st, CSA2_ERR_DEVICE_RANGE);
+              bsh = 7;
+            }
+            const float f = pow2f(-bsh);
+            *reinterpret_cast<uint4*>(kvp + kt_off(r, lane)) = bf16x8_to_f16x8_scaled(va[u][0], f);
+            *reinterpret_cast<uint4*>(kvp + kt_off(r, lane + 32)) = bf16x8_to_f16x8_scaled(va[u][1], f);
+            if (bsh != 0 && lane == 0) {
+              sKeyB[slot * kTT + r] = (uint8_t)bsh;
+              sKeyFlag[slot] = 1;
+            }
           }
         }
       }
@@ -451,7 +457,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       if (!produce(j, cwA, sbA)) break;
       if (j + 1 < nt && !produce(j + 1, cwB, sbB)) break;
     }
-    cp_async_wait<0>();
   } else if (warp < kSoftWarps) {
     // ================= softmax / O correction =================
     // S(t) is an M = 64 accumulator: head h in TMEM lane 32 (h / 16) + h % 16.
