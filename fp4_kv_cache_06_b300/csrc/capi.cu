@@ -65,7 +65,7 @@ size_t attn_group_ws_bytes(int64_t B, int H, int k, int W);
 int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                        int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, void* ws,
-                       int32_t* st, cudaStream_t s);
+                       int32_t* st, bool early, cudaStream_t s);
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -477,7 +477,8 @@ int csa2_sparse_attn(const void* q, int32_t B, int32_t H, int32_t d, const uint8
   lay.swa[0] = static_cast<const __nv_bfloat16*>(swa);
   lay.out[0] = static_cast<__nv_bfloat16*>(out);
   return launch_sparse_attn(lay, 1, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa_seq_stride, W,
-                            swa_tail != 0, 1, swa_len, softmax_scale, ws, d_status, static_cast<cudaStream_t>(stream));
+                            swa_tail != 0, 1, swa_len, softmax_scale, ws, d_status, false,
+                            static_cast<cudaStream_t>(stream));
 }
 
 static cudaEvent_t group_event(const csa2_group_args* a, int i) {
@@ -546,9 +547,11 @@ int csa2_layer_group(const csa2_group_args* a, void* stream) {
     if (!attn_layers(&lay, a->q_layers, a->swa_layers, a->out_layers, l0, L)) return CSA2_ERR_INVALID_ARG;
     // one row per sequence: the layer's SWA ring (W rows, present keys first);
     // rps rows per sequence: W + rps - 1 linear rows, each window ending at its token
+    // early: the call began with ordinary launches (the workspace zeroing or
+    // the scan), and its later kernels write only the indices and the workspace
     rc = launch_sparse_attn(lay, L, a->B, a->H, a->codes, a->scales, a->n_cap, a->n_cap, a->idx, a->k,
                             rps > 1 ? a->W + rps - 1 : a->W, a->W, rps > 1 ? 1 : 0, rps, a->swa_len,
-                            a->softmax_scale, a->ws, a->d_status, s);
+                            a->softmax_scale, a->ws, a->d_status, true, s);
     if (rc != CSA2_OK) return rc;
     // event 3 + l marks the end of the launch that holds layer l
     for (int l = l0; l < l0 + L; ++l)
@@ -611,7 +614,7 @@ int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
     AttnLayers lay;
     if (!attn_layers(&lay, a->q_layers, a->swa_layers, a->out_layers, l0, L)) return CSA2_ERR_INVALID_ARG;
     rc = launch_sparse_attn(lay, L, a->Q, a->H, a->codes, a->scales, 0, a->n_keys, a->idx, a->k, 1, a->W, 1, 1,
-                            a->swa_len, a->softmax_scale, aws, a->d_status, s);
+                            a->swa_len, a->softmax_scale, aws, a->d_status, true, s);
     if (rc != CSA2_OK) return rc;
     for (int l = l0; l < l0 + L; ++l)
       if ((rc = rec(ev(3 + l), s)) != CSA2_OK) return rc;

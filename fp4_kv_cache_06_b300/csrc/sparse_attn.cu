@@ -80,7 +80,7 @@ int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                           int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
                           float* part_ml, int splits, int tps, int32_t* st, uint64_t wait_ns, int fault,
-                          cudaStream_t s);
+                          int early, cudaStream_t s);
 
 // Split-K count for `units` = rows x layers of one launch. The attention
 // kernel runs one CTA per SM (its shared memory and all 512 TMEM columns). A
@@ -127,10 +127,15 @@ size_t attn_group_ws_bytes(int64_t B, int H, int k, int W) {
 }
 
 // Layers 0 .. L - 1 of `lay` (L <= kMaxAttnLayers) over rows 0 .. B - 1.
+// `early`: the kernels of the same call that precede this launch write only
+// `idx` (and the workspace), and the call's first kernel is an ordinary
+// launch, which begins after all earlier work on the stream: then every
+// other input was complete before the attention kernel can start, and it
+// reads them before waiting for its predecessor.
 int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
                        int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                        int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, void* ws,
-                       int32_t* st, cudaStream_t s) {
+                       int32_t* st, bool early, cudaStream_t s) {
   if (B == 0 || L == 0) return CSA2_OK;
   if (H < 1 || H > 64 || L < 0 || L > kMaxAttnLayers || B > 65535) return CSA2_ERR_UNSUPPORTED_SHAPE;
   const int64_t units = (int64_t)B * L;
@@ -146,7 +151,7 @@ int launch_sparse_attn(const AttnLayers& lay, int L, int B, int H, const uint8_t
   }
   int rc = launch_sparse_attn_tc(lay, L, B, H, codes, scales, kv_seq_stride, n_cap, idx, k, swa_seq_stride, W,
                                  swa_tail, rps < 1 ? 1 : rps, swa_len, softmax_scale, part_o, part_ml, splits, tps,
-                                 st, debug_wait_ns(), debug_fault() == kFaultAttn ? 1 : 0, s);
+                                 st, debug_wait_ns(), debug_fault() == kFaultAttn ? 1 : 0, early ? 1 : 0, s);
   if (rc != CSA2_OK || splits == 1) return rc;
   const dim3 grid((unsigned)(((kD / 4) * H + 127) / 128), (unsigned)B, (unsigned)L);
   auto kern = splits <= 4 ? k_attn_merge<4> : splits <= 8 ? k_attn_merge<8> : k_attn_merge<16>;

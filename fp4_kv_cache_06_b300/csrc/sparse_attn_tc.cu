@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     const AttnLayers lay, int H, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
     int64_t kv_seq_stride, int64_t n_cap, const int32_t* __restrict__ idx, int k, int64_t swa_seq_stride, int W,
     int swa_tail, int rps, const int32_t* __restrict__ swa_len, float scale_log2, int splits, int tiles_per_split,
-    float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st, uint64_t wait_ns, int fault) {
+    float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st, uint64_t wait_ns, int fault, int early) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;
@@ -230,7 +230,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   const int nt = max(t_end - t_begin, 0);
 
   // ---- set-up: barriers and the zero block touch no global memory and overlap
-  //      the preceding kernel; then wait for it, allocate TMEM, load Q
+  //      the preceding kernel; then wait for it, allocate TMEM, load Q.
+  //      Early launch (`early`, set when the preceding kernels of the same call
+  //      write only the Top-K indices): Q, the SWA rows, swa_len and the main KV
+  //      were complete before that call began, so everything but the index
+  //      reads runs before the wait: Q, the SWA tiles, their S and softmax.
+  //      Index reads wait (griddepcontrol.wait) in the threads that make
+  //      them, and every thread waits before the first global store.
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(kBarKvFull + i), kProd);
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   }
   for (int e = tid; e < 3 * 8192 / 16; e += kTThreads)      // P, Z, P' zero
     *reinterpret_cast<uint4*>(sp + L::kP + e * 16) = make_uint4(0, 0, 0, 0);
-  pdl_wait();
+  if (!early) pdl_wait();
   if (warp == kMmaWarp) {
     tc::tmem_alloc(base + L::kMisc, 512);
     tc::tmem_relinquish();
@@ -295,8 +301,11 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       sFp4[slot * 2 + (p >> 5)] = fp4;
     }
   };
+  // tiles 0 .. j_idx - 1 hold SWA rows only and read no index; in an early
+  // launch the producers take the row sources of tiles j_idx .. 2 after the wait
+  const int j_idx = early ? min(max(W / kTT - t_begin, 0), 3) : 3;
   if (tid < 64) {
-    for (int j = 0; j < 3 && j < nt; ++j) row_sources(j, tid);
+    for (int j = 0; j < j_idx && j < nt; ++j) row_sources(j, tid);
   }
   __syncthreads();
   cp_async_wait<0>();
@@ -357,8 +366,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         }
       }
     };
-    // one tile: returns false when the group stops
-    auto produce = [&](int j, uint2* cw, uint32_t* sb) -> bool {
+    // one tile: returns false when the group stops. `lite`: an SWA-only tile
+    // of an early launch, produced before the wait (no index work after it)
+    auto produce = [&](int j, uint2* cw, uint32_t* sb, bool lite) -> bool {
       if (named_or(kNbProd, kProd, sMisc[3] != 0)) return false;
       const int buf = j & 1, slot = j % kRing;
       unsigned char* kvp = sp + L::kKV + buf * L::kKVBytes;
@@ -443,19 +453,55 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       tc::fence_async_smem();
       // fault injection (tests of the bounded waits): the last tile is never signalled
       if (!(fault == 1 && j == nt - 1)) tc::mbar_arrive(bar(kBarKvFull + buf));
+      if (lite) return true;
       // tile j + 2's row sources were written in produce(j - 1), before this
       // call's opening barrier
       if (j + 2 < nt) prefetch(j + 2, cw, sb);
       // the row sources of tile j + 3 last: the latency of their index loads
       // then overlaps the next tile's wait for its key buffer
-      if (j + 3 < nt && p < 64) row_sources(j + 3, p);
+      if (j + 3 < nt && p < 64) {
+        pdl_wait();                                           // returns at once after the first
+        row_sources(j + 3, p);
+      }
       return true;
     };
-    if (nt > 0) prefetch(0, cwA, sbA);
-    if (nt > 1) prefetch(1, cwB, sbB);
-    for (int j = 0; j < nt; j += 2) {
-      if (!produce(j, cwA, sbA)) break;
-      if (j + 1 < nt && !produce(j + 1, cwB, sbB)) break;
+    // Tile j's FP4 rows travel in the register set of j's parity (A even, B
+    // odd). On entering the loop at tile j0, the row sources of tiles up to
+    // j0 + 2 are taken and tiles j0 and j0 + 1 are prefetched. An early launch
+    // first produces its SWA-only tiles 0 .. j_idx - 1 (with no index work),
+    // then waits for the preceding kernel and takes the row sources of tiles
+    // j_idx .. j_idx + 2.
+    int j0 = 0;
+    bool ok = true;
+    if (early) {
+      if (j_idx > 0 && nt > 0) ok = produce(0, cwA, sbA, true);
+      if (ok && j_idx > 1 && nt > 1) ok = produce(1, cwB, sbB, true);
+      j0 = min(j_idx, nt);
+      if (ok && j0 < nt) {
+        if (p < 64) {
+          pdl_wait();
+          for (int jj = j0; jj < j0 + 3 && jj < nt; ++jj) row_sources(jj, p);
+        }
+        named_sync(kNbProd, kProd);
+      }
+    }
+    if (ok && j0 < nt) {
+      if (j0 & 1) {
+        prefetch(j0, cwB, sbB);
+        if (j0 + 1 < nt) prefetch(j0 + 1, cwA, sbA);
+      } else {
+        prefetch(j0, cwA, sbA);
+        if (j0 + 1 < nt) prefetch(j0 + 1, cwB, sbB);
+      }
+    }
+    int j = j0;
+    if (ok && (j & 1) && j < nt) {                            // odd start: one tile restores the pair order
+      ok = produce(j, cwB, sbB, false);
+      ++j;
+    }
+    for (; ok && j < nt; j += 2) {
+      if (!produce(j, cwA, sbA, false)) break;
+      if (j + 1 < nt && !produce(j + 1, cwB, sbB, false)) break;
     }
   } else if (warp < kSoftWarps) {
     // ================= softmax / O correction =================
@@ -640,6 +686,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   }
   __syncthreads();
   tc::tc_fence_after();
+  if (early) pdl_wait();                        // before the first global store
   const bool have_o = nt > 0 && sMisc[3] == 0;  // uniform: read after the barrier
   if ((slen_in < 0 || slen_in > W) && split == 0 && tid == 0) report(st, CSA2_ERR_DEVICE_BOUNDS);
   if (warp < kSoftWarps && lane < 16) {
@@ -722,12 +769,12 @@ int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                           int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
                           float* part_ml, int splits, int tps, int32_t* st, uint64_t wait_ns, int fault,
-                          cudaStream_t s) {
+                          int early, cudaStream_t s) {
   dim3 grid((unsigned)splits, (unsigned)B, (unsigned)L);
   const cudaError_t e = launch_pdl(k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, lay, H, codes, scales,
                                    kv_seq_stride, n_cap, idx, k, swa_seq_stride, W, swa_tail, rps, swa_len,
                                    softmax_scale * 1.4426950408889634f, splits, tps, part_o, part_ml, st, wait_ns,
-                                   fault);
+                                   fault, early);
   count_launch();
   return launch_status(e);
 }
