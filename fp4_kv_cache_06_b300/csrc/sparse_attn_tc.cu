@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     // 16-channel group 4 pw + (lane >> 3). Per item a warp writes one 64-dim
     // block of eight consecutive rows, so the eight lanes of a store
     // wavefront hit eight distinct swizzle slots. Two register sets hold
-    // tiles j and j + 1 in flight.
+    // tiles j and j + 1 in flight (set A even tiles, set B odd ones).
     const int rl = lane & 7, g = 4 * pw + (lane >> 3);
     uint2 cwA[kItems], cwB[kItems];
     uint32_t sbA[kItems], sbB[kItems];
@@ -366,9 +366,27 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         }
       }
     };
-    // one tile: returns false when the group stops. `lite`: an SWA-only tile
-    // of an early launch, produced before the wait (no index work after it)
-    auto produce = [&](int j, uint2* cw, uint32_t* sb, bool lite) -> bool {
+    // One tile, its FP4 rows in set (cw, sb), the other set (cwo, sbo):
+    // returns false when the group stops. An early launch first produces its
+    // SWA-only tiles 0 .. j0 - 1 (`lite`: no index work after them); at tile
+    // j0 it waits for the preceding kernel and takes the row sources of tiles
+    // j0 .. j0 + 2. At tile j0, tiles j0 and j0 + 1 are prefetched. The loop
+    // below inlines this code twice, once per register set (as few copies as
+    // static register indexing allows: the instruction caches are a limit).
+    const int j0 = early ? min(j_idx, nt) : 0;
+    auto produce = [&](int j, uint2* cw, uint32_t* sb, uint2* cwo, uint32_t* sbo) -> bool {
+      const bool lite = j < j0;
+      if (j == j0) {
+        if (early) {
+          if (p < 64) {
+            pdl_wait();
+            for (int jj = j0; jj < j0 + 3 && jj < nt; ++jj) row_sources(jj, p);
+          }
+          named_sync(kNbProd, kProd);
+        }
+        prefetch(j, cw, sb);
+        if (j + 1 < nt) prefetch(j + 1, cwo, sbo);
+      }
       if (named_or(kNbProd, kProd, sMisc[3] != 0)) return false;
       const int buf = j & 1, slot = j % kRing;
       unsigned char* kvp = sp + L::kKV + buf * L::kKVBytes;
@@ -454,8 +472,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       // fault injection (tests of the bounded waits): the last tile is never signalled
       if (!(fault == 1 && j == nt - 1)) tc::mbar_arrive(bar(kBarKvFull + buf));
       if (lite) return true;
-      // tile j + 2's row sources were written in produce(j - 1), before this
-      // call's opening barrier
       if (j + 2 < nt) prefetch(j + 2, cw, sb);
       // the row sources of tile j + 3 last: the latency of their index loads
       // then overlaps the next tile's wait for its key buffer
@@ -465,43 +481,9 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       }
       return true;
     };
-    // Tile j's FP4 rows travel in the register set of j's parity (A even, B
-    // odd). On entering the loop at tile j0, the row sources of tiles up to
-    // j0 + 2 are taken and tiles j0 and j0 + 1 are prefetched. An early launch
-    // first produces its SWA-only tiles 0 .. j_idx - 1 (with no index work),
-    // then waits for the preceding kernel and takes the row sources of tiles
-    // j_idx .. j_idx + 2.
-    int j0 = 0;
-    bool ok = true;
-    if (early) {
-      if (j_idx > 0 && nt > 0) ok = produce(0, cwA, sbA, true);
-      if (ok && j_idx > 1 && nt > 1) ok = produce(1, cwB, sbB, true);
-      j0 = min(j_idx, nt);
-      if (ok && j0 < nt) {
-        if (p < 64) {
-          pdl_wait();
-          for (int jj = j0; jj < j0 + 3 && jj < nt; ++jj) row_sources(jj, p);
-        }
-        named_sync(kNbProd, kProd);
-      }
-    }
-    if (ok && j0 < nt) {
-      if (j0 & 1) {
-        prefetch(j0, cwB, sbB);
-        if (j0 + 1 < nt) prefetch(j0 + 1, cwA, sbA);
-      } else {
-        prefetch(j0, cwA, sbA);
-        if (j0 + 1 < nt) prefetch(j0 + 1, cwB, sbB);
-      }
-    }
-    int j = j0;
-    if (ok && (j & 1) && j < nt) {                            // odd start: one tile restores the pair order
-      ok = produce(j, cwB, sbB, false);
-      ++j;
-    }
-    for (; ok && j < nt; j += 2) {
-      if (!produce(j, cwA, sbA, false)) break;
-      if (j + 1 < nt && !produce(j + 1, cwB, sbB, false)) break;
+    for (int j = 0; j < nt; j += 2) {
+      if (!produce(j, cwA, sbA, cwB, sbB)) break;
+      if (j + 1 < nt && !produce(j + 1, cwB, sbB, cwA, sbA)) break;
     }
   } else if (warp < kSoftWarps) {
     // ================= softmax / O correction =================
