@@ -44,7 +44,8 @@
 // the factor goes into that head's softmax scale.
 // O for dims 0..255 accumulates in TMEM lanes 0..63 and dims 256..511 in
 // lanes 64..127 of the same 256 columns: two MMAs with A = [P; 0] and
-// A = [0; P] (zero rows leave the other half unchanged).
+// A = [0; P] (zero rows leave the other half unchanged). P is stored once,
+// between two zero blocks, and each MMA's A starts at a different block.
 // TMEM: S at columns 0..63 and 64..127 (lanes 0-15 of each quadrant), O at
 // 256..511 (512 allocated, one CTA
 // per SM). Split-K partials (m, l, unnormalised O; O stored [dim/4][head][4]
@@ -77,7 +78,7 @@ struct TcSmem {                           // offsets from a 1024-aligned base
   static constexpr int kQ = 0;                          // [8][64 heads][128 B]  64 KB
   static constexpr int kKV = kQ + 8 * 64 * 128;         // 2 x [8][64 keys][128 B]  128 KB
   static constexpr int kKVBytes = 8 * 64 * 128;
-  static constexpr int kP = kKV + 2 * kKVBytes;         // P | Z | P'  3 x 8 KB
+  static constexpr int kP = kKV + 2 * kKVBytes;         // Z | P | Z  3 x 8 KB
   static constexpr int kSrc = kP + 3 * 8192;            // int64 [kRing][64]: >= 0 FP4 row, -1 absent, <= -2 SWA row
   static constexpr int kMask = kSrc + kRing * kTT * 8;  // u32 [kRing][2] valid keys
   static constexpr int kFp4 = kMask + kRing * 8;        // u32 [kRing][2] keys that are FP4 rows
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       if (j > 0) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1, wait_ns) && ok;
       if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      unsigned char* prow = sp + L::kP + h * 128;
+      unsigned char* prow = sp + L::kP + 8192 + h * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[4];
@@ -568,8 +569,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         const uint4 v4 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         const int sw = (((4 * half + c) ^ (h & 7)) << 4);
         if (h < H) {
-          *reinterpret_cast<uint4*>(prow + sw) = v4;               // P  (rows 0..63 of [P; Z])
-          *reinterpret_cast<uint4*>(prow + 16384 + sw) = v4;       // P' (rows 64..127 of [Z; P'])
+          *reinterpret_cast<uint4*>(prow + sw) = v4;               // rows 0..63 of [P; Z], 64..127 of [Z; P]
         }
       }
       l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
@@ -609,8 +609,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         const uint32_t kv = base + L::kKV + (j & 1) * L::kKVBytes;
 #pragma unroll
         for (int ks = 0; ks < kTT / 16; ++ks) {
-          const uint64_t a0 = tc::smem_desc(base + L::kP + ks * 32, 16, 1024, tc::kSwizzle128B);
-          const uint64_t a1 = tc::smem_desc(base + L::kP + 8192 + ks * 32, 16, 1024, tc::kSwizzle128B);
+          const uint64_t a0 = tc::smem_desc(base + L::kP + 8192 + ks * 32, 16, 1024, tc::kSwizzle128B);   // [P; Z]
+          const uint64_t a1 = tc::smem_desc(base + L::kP + ks * 32, 16, 1024, tc::kSwizzle128B);          // [Z; P]
           const uint64_t b0 = tc::smem_desc(kv + ks * 2048, 8192, 1024, tc::kSwizzle128B);
           const uint64_t b1 = tc::smem_desc(kv + 4 * 8192 + ks * 2048, 8192, 1024, tc::kSwizzle128B);
           tc::mma_f16(tmem + kTOcol, a0, b0, idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
