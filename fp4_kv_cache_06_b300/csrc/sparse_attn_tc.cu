@@ -197,6 +197,36 @@ __device__ __forceinline__ uint32_t ldg_hint_u8(const void* p, uint64_t pol) {
   return v;
 }
 
+// 2^((s0 - m) * sl) and 2^((s1 - m) * sl): the subtraction and the scaling as
+// two fp32x2 operations (each lane rounds as the scalar form), then the
+// hardware base-2 exponential (PTX ex2.approx.ftz: relative error about
+// 2^-22, results below 2^-126 flushed to zero; P is rounded to fp16 next).
+__device__ __forceinline__ void exp2_pair(uint32_t s0, uint32_t s1, uint64_t negm2, uint64_t sl2, float& p0,
+                                          float& p1) {
+  asm("{\n .reg .b64 d;\n .reg .f32 a, b;\n"
+      " mov.b64 d, {%2, %3};\n add.rn.f32x2 d, d, %4;\n mul.rn.f32x2 d, d, %5;\n"
+      " mov.b64 {a, b}, d;\n ex2.approx.ftz.f32 %0, a;\n ex2.approx.ftz.f32 %1, b;\n}"
+      : "=f"(p0), "=f"(p1) : "r"(s0), "r"(s1), "l"(negm2), "l"(sl2));
+}
+// acc += the two fp16 values of h2, as one fp32x2 addition
+__device__ __forceinline__ uint64_t add_half2(uint64_t acc, uint32_t h2) {
+  asm("{\n .reg .b16 lo, hi;\n .reg .f32 a, b;\n .reg .b64 p;\n"
+      " mov.b32 {lo, hi}, %1;\n cvt.f32.f16 a, lo;\n cvt.f32.f16 b, hi;\n"
+      " mov.b64 p, {a, b};\n add.rn.f32x2 %0, %0, p;\n}"
+      : "+l"(acc) : "r"(h2));
+  return acc;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float hsum_f32x2(uint64_t a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo + hi;
+}
+
 __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     const AttnLayers lay, int H, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
     int64_t kv_seq_stride, int64_t n_cap, const int32_t* __restrict__ idx, int k, int64_t swa_seq_stride, int W,
@@ -545,7 +575,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       // P and O are free once PV(j - 1) has finished
       if (j > 0) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1, wait_ns) && ok;
       if (!ok) { report(st, CSA2_ERR_TIMEOUT); sMisc[3] = 1; }
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};            // pairs of fp32 partial sums
+      const uint64_t negm2 = pack_f32x2(-mref, -mref), sl2 = pack_f32x2(sl, sl);
       unsigned char* prow = sp + L::kP + 8192 + h * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -553,18 +584,22 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int x = 8 * c + 2 * u;
-          float p0 = exp2f((__uint_as_float(r[x]) - mref) * sl), p1 = exp2f((__uint_as_float(r[x + 1]) - mref) * sl);
-          int b0 = 0, b1 = 0;
+          float p0, p1;
+          exp2_pair(r[x], r[x + 1], negm2, sl2, p0, p1);
           if (kscaled) {                      // a scaled row's value enters PV as 2^-b v: its P as 2^b P
-            b0 = (int)((bw[x >> 2] >> (8 * (x & 3))) & 0xFF);
-            b1 = (int)((bw[(x + 1) >> 2] >> (8 * ((x + 1) & 3))) & 0xFF);
-            p0 *= pow2f(b0);
-            p1 *= pow2f(b1);
+            const int b0 = (int)((bw[x >> 2] >> (8 * (x & 3))) & 0xFF);
+            const int b1 = (int)((bw[(x + 1) >> 2] >> (8 * ((x + 1) & 3))) & 0xFF);
+            const __half2 pv = __floats2half2_rn(p0 * pow2f(b0), p1 * pow2f(b1));
+            const float2 f = __half22float2(pv);
+            float lo, hi;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(sum2[u]));
+            sum2[u] = pack_f32x2(lo + f.x * pow2f(-b0), hi + f.y * pow2f(-b1));
+            pk[u] = *reinterpret_cast<const uint32_t*>(&pv);
+          } else {
+            const __half2 pv = __floats2half2_rn(p0, p1);
+            pk[u] = *reinterpret_cast<const uint32_t*>(&pv);
+            sum2[u] = add_half2(sum2[u], pk[u]);
           }
-          const __half2 pv = __floats2half2_rn(p0, p1);
-          const float2 f = __half22float2(pv);
-          sum[u] += kscaled ? f.x * pow2f(-b0) + f.y * pow2f(-b1) : f.x + f.y;
-          pk[u] = *reinterpret_cast<const uint32_t*>(&pv);
         }
         const uint4 v4 = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         const int sw = (((4 * half + c) ^ (h & 7)) << 4);
@@ -572,7 +607,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
           *reinterpret_cast<uint4*>(prow + sw) = v4;               // rows 0..63 of [P; Z], 64..127 of [Z; P]
         }
       }
-      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      l_run = l_run * alpha + ((hsum_f32x2(sum2[0]) + hsum_f32x2(sum2[1])) + (hsum_f32x2(sum2[2]) + hsum_f32x2(sum2[3])));
       if (half == 0) sAlpha[h] = alpha;
       if (alpha != 1.f && j > 0) sMisc[1 + (j & 1)] = 1;
       named_sync(kNbSoft, kSoftThreads);
