@@ -613,8 +613,11 @@ int csa2_prefill_group(const csa2_prefill_args* a, void* stream) {
     const int L = n_layers - l0 < kMaxAttnLayers ? n_layers - l0 : kMaxAttnLayers;
     AttnLayers lay;
     if (!attn_layers(&lay, a->q_layers, a->swa_layers, a->out_layers, l0, L)) return CSA2_ERR_INVALID_ARG;
+    // not early: the selection kernels before it are ordinary launches, so
+    // the attention starts only after they end, and an early launch would
+    // only move its index reads behind the window tiles
     rc = launch_sparse_attn(lay, L, a->Q, a->H, a->codes, a->scales, 0, a->n_keys, a->idx, a->k, 1, a->W, 1, 1,
-                            a->swa_len, a->softmax_scale, aws, a->d_status, true, s);
+                            a->swa_len, a->softmax_scale, aws, a->d_status, false, s);
     if (rc != CSA2_OK) return rc;
     for (int l = l0; l < l0 + L; ++l)
       if ((rc = rec(ev(3 + l), s)) != CSA2_OK) return rc;
