@@ -19,14 +19,14 @@
 //             scale as a packed f16 multiply: the product, <= 6 significant
 //             bits in 2^-10 .. 2688, is exact in fp16) into one of two key
 //             buffers in the K-major 128-byte-swizzle layout
-//             [dim/64][key][128 B]. SWA rows (bf16) are loaded into
-//             registers, four rows per warp in flight, converted there and
-//             stored once; a row whose largest magnitude
-//             reaches 2^16 is first scaled by 2^-b (b <= 7, exact), and its
-//             logits and probabilities are scaled back by 2^b in the softmax
-//             (rows reaching 2^23 are reported as out of range). Below 2^-14
-//             a value keeps an absolute accuracy of 2^-25; absent rows are
-//             zero;
+//             [dim/64][key][128 B]. SWA rows (bf16) arrive in that layout
+//             by TMA (one 2-D load per dim block of 64 rows; tile 0's is
+//             issued at set-up) and are converted in place; a row whose
+//             largest magnitude reaches 2^16 is first scaled by 2^-b (b <= 7,
+//             exact), and its logits and probabilities are scaled back by 2^b
+//             in the softmax (rows reaching 2^23 are reported as out of
+//             range). Below 2^-14 a value keeps an absolute accuracy of
+//             2^-25; absent rows are zero;
 //   MMA (one thread each of warps 12 and 13): warp 12 issues
 //             S(t) = Q K(t)^T with tcgen05.mma kind::f16, M = 64 heads,
 //             N = 64 keys, K = 512, into one of two S buffers in TMEM, as
@@ -54,6 +54,8 @@
 // timed-out wait the CTA reports CSA2_ERR_TIMEOUT and winds down (the warp
 // groups decide to stop by barrier reductions, so no warp is left behind at
 // a barrier).
+#include <cstring>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -103,7 +105,8 @@ constexpr int kBarODone = 7;              // PV done (tcgen05.commit)
 constexpr int kBarFin = 8;                // every MMA of the CTA done (tcgen05.commit)
 constexpr int kBarQ = 9;                  // Q converted (every thread of the converting warps arrives)
 constexpr int kBarSFree = 10;             // [2] S buffer read by the softmax (the PV warp arrives)
-constexpr int kBarSFin = 12;              // every S MMA done (tcgen05.commit of the S warp)
+constexpr int kBarSFin = 12;
+constexpr int kBarWin = 13;               // [2] window rows of key buffer i landed (TMA, expect_tx)              // every S MMA done (tcgen05.commit of the S warp)
 constexpr int kQWarps = kSoftWarps + 2;   // the softmax warps and the two MMA warps convert Q
 
 __device__ __forceinline__ uint32_t kt_off(int row, int chunk) {     // chunk = 16-byte unit of 8 dims
@@ -185,12 +188,6 @@ __device__ __forceinline__ uint2 ldg_hint_u2(const void* p, uint64_t pol) {
   asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
   return v;
 }
-__device__ __forceinline__ uint4 ldg_hint_u4(const void* p, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
-  return v;
-}
 __device__ __forceinline__ uint32_t ldg_hint_u8(const void* p, uint64_t pol) {
   uint16_t v;
   asm volatile("ld.global.nc.L2::cache_hint.u8 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
@@ -227,8 +224,15 @@ __device__ __forceinline__ float hsum_f32x2(uint64_t a) {
   return lo + hi;
 }
 
+// One 2-D tensor map per layer over its SWA rows ([rows][1024 B], box 64
+// rows x 128 B, 128-byte swizzle): one load of a dim block of 64 window rows
+// lands in the key-buffer layout.
+struct SwaMaps {
+  CUtensorMap m[kMaxAttnLayers];
+};
+
 __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
-    const AttnLayers lay, int H, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+    const AttnLayers lay, const __grid_constant__ SwaMaps swa_maps, int H, const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
     int64_t kv_seq_stride, int64_t n_cap, const int32_t* __restrict__ idx, int k, int64_t swa_seq_stride, int W,
     int swa_tail, int rps, const int32_t* __restrict__ swa_len, float scale_log2, int splits, int tiles_per_split,
     float* __restrict__ part_o, float* __restrict__ part_ml, int32_t* st, uint64_t wait_ns, int fault, int early) {
@@ -251,7 +255,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
 
   const int b = blockIdx.y, split = blockIdx.x, layer = blockIdx.z;
   const __nv_bfloat16* __restrict__ q = lay.q[layer];
-  const __nv_bfloat16* __restrict__ swa = lay.swa[layer];
   __nv_bfloat16* __restrict__ out = lay.out[layer];
   const int64_t unit = (int64_t)layer * gridDim.y + b;     // (layer, row) of the partials
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -281,10 +284,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     tc::mbar_init(bar(kBarSFree), 1);
     tc::mbar_init(bar(kBarSFree + 1), 1);
     tc::mbar_init(bar(kBarSFin), 1);
+    tc::mbar_init(bar(kBarWin), 1);
+    tc::mbar_init(bar(kBarWin + 1), 1);
     tc::fence_barrier_init();
     sMisc[1] = 0;
     sMisc[2] = 0;
     sMisc[3] = 0;
+    sMisc[4] = 0;                                             // window loads issued (bit per key buffer)
   }
   for (int e = tid; e < 3 * 8192 / 16; e += kTThreads)      // P, Z, P' zero
     *reinterpret_cast<uint4*>(sp + L::kP + e * 16) = make_uint4(0, 0, 0, 0);
@@ -308,6 +314,23 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   const int64_t kv_row0 = (int64_t)(b / rps) * kv_seq_stride;
   const int64_t swa_row0 = (int64_t)(b / rps) * swa_seq_stride + (b % rps);
   const int slen = min(max(slen_in, 0), W);
+  // Window tiles (local tiles 0 .. j_win - 1 hold window slots r < W): their
+  // rows come by TMA, one dim block (64 rows x 128 B) per load, into the key
+  // buffer of the tile: tile 0's now (key buffer 0 is free), tile 1's once Q
+  // has left key buffer 1. Rows past the window or the buffer are zeroed or
+  // overwritten by the producers after the load.
+  const int j_win = min(max((W + kTT - 1) / kTT - t_begin, 0), 2);
+  auto window_load = [&](int j) {                             // one thread
+    const int buf = j & 1;
+    const int64_t y = swa_row0 + (swa_tail ? W - slen : 0) + (int64_t)(t_begin + j) * kTT;
+    atomicOr(const_cast<uint32_t*>(&sMisc[4]), 1u << buf);
+    tc::mbar_expect_tx(bar(kBarWin + buf), 8 * 8192);
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+      tc::tma_load_2d(base + L::kKV + buf * L::kKVBytes + d * 8192, &swa_maps.m[layer], d * 128, (int32_t)y,
+                      bar(kBarWin + buf));
+  };
+  if (tid == 0 && j_win > 0 && nt > 0) window_load(0);
 
   // Row sources of tile j (called by a whole warp pair: row p of the tile).
   // Key slot r < W is SWA row r (present if r < slen); slot W + i is Top-K entry i.
@@ -431,7 +454,14 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         report(st, CSA2_ERR_TIMEOUT);
         sMisc[3] = 1;
       }
-      const int64_t* src = sSrc + slot * kTT;
+      // a window tile's rows land by TMA before anything else is written there
+      if (j < j_win) {
+        if (j == 1 && p == 0) window_load(1);                 // Q has left key buffer 1
+        if (!tc::mbar_wait(bar(kBarWin + buf), 0, wait_ns)) {
+          report(st, CSA2_ERR_TIMEOUT);
+          sMisc[3] = 1;
+        }
+      }
       const uint64_t valid = (uint64_t)sMask[slot * 2] | ((uint64_t)sMask[slot * 2 + 1] << 32);
       const uint64_t fp4 = (uint64_t)sFp4[slot * 2] | ((uint64_t)sFp4[slot * 2 + 1] << 32);
       const uint64_t swa_rows = valid & ~fp4;
@@ -459,43 +489,30 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
         *reinterpret_cast<uint4*>(kvp + kt_off(r, 2 * g)) = make_uint4(o[0], o[1], o[2], o[3]);
         *reinterpret_cast<uint4*>(kvp + kt_off(r, 2 * g + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
       }
-      // SWA rows: bf16 from global memory into registers (four rows of a warp
-      // in flight), converted there and stored once as fp16. A row whose
-      // largest magnitude reaches 2^16 (beyond fp16) is scaled by 2^-b first
-      // (b = its binary exponent - 15, at most 7: rows reaching 2^23
-      // saturate and are reported); b goes to the softmax through kKeyB.
+      // SWA rows: bf16 -> fp16 in place (each lane two 16-byte chunks of a
+      // row). A row whose largest magnitude reaches 2^16 (beyond fp16) is
+      // scaled by 2^-b first (b = its binary exponent - 15, at most 7: rows
+      // reaching 2^23 saturate and are reported); b goes to the softmax
+      // through kKeyB.
       if (swa_rows) {
-#pragma unroll 1
-        for (int r0 = pw; r0 < kTT; r0 += 4 * kProdWarps) {
-          uint4 va[4][2];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int r = r0 + u * kProdWarps;
-            va[u][0] = make_uint4(0, 0, 0, 0);
-            va[u][1] = va[u][0];
-            if (r < kTT && ((swa_rows >> r) & 1)) {
-              const __nv_bfloat16* row = swa + (-2 - src[r]) * kTD;
-              va[u][0] = ldg_hint_u4(row + lane * 8, pol_stream);
-              va[u][1] = ldg_hint_u4(row + (lane + 32) * 8, pol_stream);
-            }
+#pragma unroll 2
+        for (int r = pw; r < kTT; r += kProdWarps) {
+          if (!((swa_rows >> r) & 1)) continue;                 // warp-uniform
+          uint4* p0 = reinterpret_cast<uint4*>(kvp + kt_off(r, lane));
+          uint4* p1 = reinterpret_cast<uint4*>(kvp + kt_off(r, lane + 32));
+          const uint4 v0 = *p0, v1 = *p1;
+          const int e = (int)(__reduce_max_sync(0xffffffffu, bf16x16_max_mag(v0, v1)) >> 7) - 127;
+          int bsh = e >= 16 ? e - 15 : 0;
+          if (bsh > 7) {
+            if (lane == 0) report(st, CSA2_ERR_DEVICE_RANGE);
+            bsh = 7;
           }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int r = r0 + u * kProdWarps;
-            if (r >= kTT || !((swa_rows >> r) & 1)) continue;       // warp-uniform
-            const int e = (int)(__reduce_max_sync(0xffffffffu, bf16x16_max_mag(va[u][0], va[u][1])) >> 7) - 127;
-            int bsh = e >= 16 ? e - 15 : 0;
-            if (bsh > 7) {
-              if (lane == 0) report(st, CSA2_ERR_DEVICE_RANGE);
-              bsh = 7;
-            }
-            const float f = pow2f(-bsh);
-            *reinterpret_cast<uint4*>(kvp + kt_off(r, lane)) = bf16x8_to_f16x8_scaled(va[u][0], f);
-            *reinterpret_cast<uint4*>(kvp + kt_off(r, lane + 32)) = bf16x8_to_f16x8_scaled(va[u][1], f);
-            if (bsh != 0 && lane == 0) {
-              sKeyB[slot * kTT + r] = (uint8_t)bsh;
-              sKeyFlag[slot] = 1;
-            }
+          const float f = pow2f(-bsh);
+          *p0 = bf16x8_to_f16x8_scaled(v0, f);
+          *p1 = bf16x8_to_f16x8_scaled(v1, f);
+          if (bsh != 0 && lane == 0) {
+            sKeyB[slot * kTT + r] = (uint8_t)bsh;
+            sKeyFlag[slot] = 1;
           }
         }
       }
@@ -767,6 +784,13 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       part_ml[pidx * 2 + 1] = sL[h];
     }
   }
+  // no window load may still be in flight when the CTA exits (a group that
+  // stopped early may not have waited for one)
+  if (tid == 0) {
+    const uint32_t issued = sMisc[4];
+    for (int i = 0; i < 2; ++i)
+      if ((issued >> i) & 1) (void)tc::mbar_wait(bar(kBarWin + i), 0, wait_ns);
+  }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
@@ -782,13 +806,23 @@ int attn_tc_init_attributes() {
   return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
+bool make_tmap_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows);
+
 int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                           int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
                           float* part_ml, int splits, int tps, int32_t* st, uint64_t wait_ns, int fault,
                           int early, cudaStream_t s) {
   dim3 grid((unsigned)splits, (unsigned)B, (unsigned)L);
-  const cudaError_t e = launch_pdl(k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, lay, H, codes, scales,
+  // each layer's window rows as a 2-D tensor up to the last row's window end
+  SwaMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (W > 0) {
+    const uint64_t rows = (uint64_t)((B - 1) / rps) * (uint64_t)swa_seq_stride + (uint64_t)((B - 1) % rps) + (uint64_t)W;
+    for (int l = 0; l < L; ++l)
+      if (!make_tmap_rows128(&maps.m[l], lay.swa[l], rows, (uint64_t)kTD * 2, kTT)) return CSA2_ERR_CUDA;
+  }
+  const cudaError_t e = launch_pdl(k_sparse_attn_tc, grid, dim3(kTThreads), TcSmem::kBytes, s, lay, maps, H, codes, scales,
                                    kv_seq_stride, n_cap, idx, k, swa_seq_stride, W, swa_tail, rps, swa_len,
                                    softmax_scale * 1.4426950408889634f, splits, tps, part_o, part_ml, st, wait_ns,
                                    fault, early);
