@@ -114,6 +114,55 @@ def test_prefill_layout_shared_cache_and_sliding_rows():
     check_attn(out, ref)
 
 
+@pytest.mark.parametrize("W", [0, 17, 64, 100])
+def test_sparse_attn_window_sizes(W):
+    """Windows that are not a multiple of the 64-key tile: a tile then holds
+    window rows and gathered rows together (W = 17, 100), one tile is window
+    only (W = 64), or there is no window (W = 0). The window rows of a tile
+    are loaded whole by TMA; the rows past the window or past the ring's
+    filled slots must not leak into the result."""
+    B, H, k, n = 3, 32, 256, 700
+    kv, codes, scales = _cache(B, n, seed=300 + W)
+    rng = np.random.default_rng(300 + W)
+    idx = np.stack([np.sort(rng.permutation(n)[:k]) for _ in range(B)]).astype(np.int32)
+    idx[1, k // 2:] = -1                                      # a partly absent row
+    swa_len = np.array([W, min(W, 5), W // 2], dtype=np.int32)
+    q = synth.normal_bf16((B, H, 512), seed=31, stream="q").to(DEV)
+    # ring slots past swa_len hold other data, which must be ignored
+    swa = (synth.normal_bf16((B, max(W, 1), 512), seed=32, stream="swa") * 3).to(DEV)[:, :W]
+    out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, B, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa.contiguous(),
+                          torch.from_numpy(swa_len).to(DEV), out, ws, W=W)
+    torch.cuda.synchronize()
+    kvb, qb, swab = bits16(kv), bits16(q), bits16(swa.contiguous())
+    ref = np.stack([oracle.sparse_attention(qb[b], *oracle.quantize_fp4(kvb[b]), idx[b], swab[b], swa_len[b])
+                    for b in range(B)])
+    check_attn(out, ref)
+
+
+def test_prefill_layout_window_not_a_tile_multiple():
+    """Prefill form with W = 100 and short windows at the start of a chunk:
+    query i's window is the last swa_len of rows i .. i + W - 1."""
+    Q, H, k, n, W = 24, 64, 256, 900, 100
+    kv, codes, scales = _cache(1, n, seed=41)
+    rng = np.random.default_rng(41)
+    idx = np.stack([np.sort(rng.permutation(n)[:k]) for _ in range(Q)]).astype(np.int32)
+    q = synth.normal_bf16((Q, H, 512), seed=41, stream="q").to(DEV)
+    swa_rows = synth.normal_bf16((Q + W - 1, 512), seed=41, stream="swa").to(DEV)
+    slen = np.minimum(np.arange(Q) * 9 + 1, W).astype(np.int32)
+    out = torch.empty((Q, H, 512), dtype=torch.bfloat16, device=DEV)
+    ws = csa2.alloc_workspace(csa2.workspace_size(csa2.OP_SPARSE_ATTN, Q, 0, k, 2048, H))
+    csa2.csa2_sparse_attn(q, codes, scales, torch.from_numpy(idx).to(DEV), swa_rows, torch.from_numpy(slen).to(DEV),
+                          out, ws, kv_seq_stride=0, swa_seq_stride=1, W=W, swa_tail=True)
+    torch.cuda.synchronize()
+    c, s = oracle.quantize_fp4(bits16(kv)[0])
+    sb, qb = bits16(swa_rows), bits16(q)
+    ref = np.stack([oracle.sparse_attention(qb[i], c, s, idx[i], sb[i + W - slen[i]:i + W], slen[i])
+                    for i in range(Q)])
+    check_attn(out, ref)
+
+
 def test_sparse_attn_exact_over_the_bf16_range():
     """Queries and SWA rows far outside fp16's range (|x| up to 1e5) and far
     below it (|x| ~ 1e-6), mixed per head and per row. Each query head is
