@@ -138,10 +138,10 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float f) {
 // non-negative values order like the values).
 __device__ __forceinline__ uint32_t bf16x16_max_mag(uint4 a, uint4 b) {
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint32_t m = 0;
+  uint32_t m = 0;                                   // two 16-bit lanes: the magnitudes' bit patterns
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-  return m;
+  for (int i = 0; i < 8; ++i) asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(w[i] & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
 }
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }   // |e| <= 126
 
@@ -507,9 +507,14 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
             if (lane == 0) report(st, CSA2_ERR_DEVICE_RANGE);
             bsh = 7;
           }
-          const float f = pow2f(-bsh);
-          *p0 = bf16x8_to_f16x8_scaled(v0, f);
-          *p1 = bf16x8_to_f16x8_scaled(v1, f);
+          if (bsh == 0) {                                       // the common case: no scale
+            *p0 = bf16x8_to_f16x8(v0);
+            *p1 = bf16x8_to_f16x8(v1);
+          } else {
+            const float f = pow2f(-bsh);
+            *p0 = bf16x8_to_f16x8_scaled(v0, f);
+            *p1 = bf16x8_to_f16x8_scaled(v1, f);
+          }
           if (bsh != 0 && lane == 0) {
             sKeyB[slot * kTT + r] = (uint8_t)bsh;
             sKeyFlag[slot] = 1;
