@@ -124,14 +124,17 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// The same, each value first multiplied by f (a power of two: exact).
+// The same, each value first multiplied by f (a power of two: exact), the
+// two values of a pair by one fp32x2 multiply.
 __device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float f) {
   uint32_t in[4] = {v.x, v.y, v.z, v.w}, o[4];
+  uint64_t f2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(f2) : "f"(f));
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(in[i] << 16) * f, hi = __uint_as_float(in[i] & 0xFFFF0000u) * f;
-    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(hi), "f"(lo));
-  }
+  for (int i = 0; i < 4; ++i)
+    asm("{\n .reg .b64 d;\n .reg .f32 a, b;\n mov.b64 d, {%1, %2};\n mul.rn.f32x2 d, d, %3;\n"
+        " mov.b64 {a, b}, d;\n cvt.rn.satfinite.f16x2.f32 %0, b, a;\n}"
+        : "=r"(o[i]) : "r"(in[i] << 16), "r"(in[i] & 0xFFFF0000u), "l"(f2));
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 // Largest magnitude bit pattern of 16 bf16 values (bit patterns of
