@@ -20,8 +20,8 @@
 //             bits in 2^-10 .. 2688, is exact in fp16) into one of two key
 //             buffers in the K-major 128-byte-swizzle layout
 //             [dim/64][key][128 B]. SWA rows (bf16) arrive in that layout
-//             by TMA (one 2-D load per dim block of 64 rows; tile 0's is
-//             issued at set-up) and are converted in place; a row whose
+//             by TMA (one 2-D load per dim block of 64 rows, issued at
+//             set-up) and are converted in place; a row whose
 //             largest magnitude reaches 2^16 is first scaled by 2^-b (b <= 7,
 //             exact), and its logits and probabilities are scaled back by 2^b
 //             in the softmax (rows reaching 2^23 are reported as out of
@@ -191,6 +191,12 @@ __device__ __forceinline__ uint2 ldg_hint_u2(const void* p, uint64_t pol) {
   asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;" : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
   return v;
 }
+__device__ __forceinline__ uint4 ldg_hint_u4(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+  return v;
+}
 __device__ __forceinline__ uint32_t ldg_hint_u8(const void* p, uint64_t pol) {
   uint16_t v;
   asm volatile("ld.global.nc.L2::cache_hint.u8 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
@@ -303,13 +309,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     tc::tmem_relinquish();
   }
   const uint64_t pol_keep = l2_evict_last(), pol_stream = l2_evict_first();
-  for (int e = tid; e < 64 * 64; e += kTThreads) {          // Q rows (bf16) staged in key buffer 1
-    const int h = e >> 6, c = e & 63;
-    if (h < H)
-      cp_async16_hint(base + L::kKV + L::kKVBytes + kt_off(h, c), q + ((int64_t)b * H + h) * kTD + c * 8,
-                      pol_stream);
-  }
-  cp_async_commit();
   // the SWA length is clamped without a branch, so nothing waits on its load
   const int slen_in = swa_len[b];
   // row b reads the caches of sequence b / rps; with rps > 1 the sequence's
@@ -319,9 +318,8 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
   const int slen = min(max(slen_in, 0), W);
   // Window tiles (local tiles 0 .. j_win - 1 hold window slots r < W): their
   // rows come by TMA, one dim block (64 rows x 128 B) per load, into the key
-  // buffer of the tile: tile 0's now (key buffer 0 is free), tile 1's once Q
-  // has left key buffer 1. Rows past the window or the buffer are zeroed or
-  // overwritten by the producers after the load.
+  // buffer of the tile, both issued here. Rows past the window or the buffer
+  // are zeroed or overwritten by the producers after the load.
   const int j_win = min(max((W + kTT - 1) / kTT - t_begin, 0), 2);
   auto window_load = [&](int j) {                             // one thread
     const int buf = j & 1;
@@ -334,6 +332,7 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
                       bar(kBarWin + buf));
   };
   if (tid == 0 && j_win > 0 && nt > 0) window_load(0);
+  if (tid == 0 && j_win > 1 && nt > 1) window_load(1);
 
   // Row sources of tile j (called by a whole warp pair: row p of the tile).
   // Key slot r < W is SWA row r (present if r < slen); slot W + i is Top-K entry i.
@@ -365,30 +364,41 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
     for (int j = 0; j < j_idx && j < nt; ++j) row_sources(j, tid);
   }
   __syncthreads();
-  cp_async_wait<0>();
-  __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sMisc[0];
   pdl_trigger();                              // TMEM is held: the next kernel may start launching
   // Q -> fp16, one warp per head: scaled by 2^-a so that the head's largest
   // magnitude lies in [2^14, 2^15) (heads >= H and all-zero heads: a = 0).
-  // The softmax warps and the two MMA warps do this while the producers
-  // start on tile 0; tile 1 goes into key buffer 1 (the bf16 staging of Q) only after
-  // every converting warp has arrived on kBarQ, and S and the softmax wait
-  // for it too.
+  // The softmax warps and the two MMA warps read Q's rows from global memory
+  // (four heads of a warp in flight) and write them converted, while the
+  // producers start on the window tiles; S and the softmax wait on kBarQ.
   if (warp < kSoftWarps || warp >= kMmaWarp) {
-    for (int h = warp < kSoftWarps ? warp : kSoftWarps + (warp - kMmaWarp); h < 64; h += kQWarps) {
-      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-      if (h < H) {
-        v0 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane));
-        v1 = *reinterpret_cast<const uint4*>(sp + L::kKV + L::kKVBytes + kt_off(h, lane + 32));
+    const int h_first = warp < kSoftWarps ? warp : kSoftWarps + (warp - kMmaWarp);
+#pragma unroll 1
+    for (int h0 = h_first; h0 < 64; h0 += 4 * kQWarps) {
+      uint4 v[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int h = h0 + u * kQWarps;
+        v[u][0] = make_uint4(0, 0, 0, 0);
+        v[u][1] = v[u][0];
+        if (h < H) {                                          // H <= 64
+          const __nv_bfloat16* qrow = q + ((int64_t)b * H + h) * kTD;
+          v[u][0] = ldg_hint_u4(qrow + lane * 8, pol_stream);
+          v[u][1] = ldg_hint_u4(qrow + (lane + 32) * 8, pol_stream);
+        }
       }
-      const uint32_t mx = __reduce_max_sync(0xffffffffu, bf16x16_max_mag(v0, v1));
-      const int a = mx == 0 ? 0 : min(max((int)(mx >> 7) - 127 - 14, -100), 100);
-      const float f = pow2f(-a);
-      *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane)) = bf16x8_to_f16x8_scaled(v0, f);
-      *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane + 32)) = bf16x8_to_f16x8_scaled(v1, f);
-      if (lane == 0) sQScale[h] = pow2f(a);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int h = h0 + u * kQWarps;
+        if (h >= 64) break;                                   // warp-uniform
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, bf16x16_max_mag(v[u][0], v[u][1]));
+        const int a = mx == 0 ? 0 : min(max((int)(mx >> 7) - 127 - 14, -100), 100);
+        const float f = pow2f(-a);
+        *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane)) = bf16x8_to_f16x8_scaled(v[u][0], f);
+        *reinterpret_cast<uint4*>(sp + L::kQ + kt_off(h, lane + 32)) = bf16x8_to_f16x8_scaled(v[u][1], f);
+        if (lane == 0) sQScale[h] = pow2f(a);
+      }
     }
     tc::fence_async_smem();
     tc::mbar_arrive(bar(kBarQ));
@@ -447,11 +457,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       if (named_or(kNbProd, kProd, sMisc[3] != 0)) return false;
       const int buf = j & 1, slot = j % kRing;
       unsigned char* kvp = sp + L::kKV + buf * L::kKVBytes;
-      // key buffer 1 held the bf16 Q until the converting warps were done
-      if (j == 1 && !tc::mbar_wait(bar(kBarQ), 0, wait_ns)) {
-        report(st, CSA2_ERR_TIMEOUT);
-        sMisc[3] = 1;
-      }
       // the buffer is free once PV(j - 2) has finished
       if (j >= 2 && !tc::mbar_wait(bar(kBarKvEmpty + buf), ((j >> 1) - 1) & 1, wait_ns)) {
         report(st, CSA2_ERR_TIMEOUT);
@@ -459,7 +464,6 @@ __global__ void __launch_bounds__(kTThreads, 1) k_sparse_attn_tc(
       }
       // a window tile's rows land by TMA before anything else is written there
       if (j < j_win) {
-        if (j == 1 && p == 0) window_load(1);                 // Q has left key buffer 1
         if (!tc::mbar_wait(bar(kBarWin + buf), 0, wait_ns)) {
           report(st, CSA2_ERR_TIMEOUT);
           sMisc[3] = 1;
