@@ -299,8 +299,6 @@ __global__ void __launch_bounds__(kTmaThreads, 2) k_index_scan_tma(
   if (R == 1 && hist) topk_hist_flush(sh_hist, hist + (int64_t)b * kHistBins, hdr + b, topk_k, gridDim.x);
 }
 
-bool make_tmap_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows);
-
 static int tma_scan_init = 0;
 int scan_init_attributes() {
   for (auto kern : {k_index_scan_tma<1>, k_index_scan_tma<2>, k_index_scan_tma<4>, k_index_scan_tma<8>})

@@ -818,8 +818,6 @@ int attn_tc_init_attributes() {
   return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }
 
-bool make_tmap_rows128(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows);
-
 int launch_sparse_attn_tc(const AttnLayers& lay, int L, int B, int H, const uint8_t* codes, const uint8_t* scales,
                           int64_t kv_seq_stride, int64_t n_cap, const int32_t* idx, int k, int64_t swa_seq_stride,
                           int W, int swa_tail, int rps, const int32_t* swa_len, float softmax_scale, float* part_o,
