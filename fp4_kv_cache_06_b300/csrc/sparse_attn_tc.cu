@@ -14,19 +14,18 @@
 // the gathered rows) by a warp-specialised pipeline:
 //   producers (warps 4-11): row sources from the Top-K indices three tiles
 //             ahead; the FP4 rows prefetched into registers two tiles ahead,
-//             then
-//             dequantised (E2M1 -> f16x2 hardware convert times the E4M3
-//             scale as a packed f16 multiply: the product, <= 6 significant
-//             bits in 2^-10 .. 2688, is exact in fp16) into one of two key
-//             buffers in the K-major 128-byte-swizzle layout
-//             [dim/64][key][128 B]. SWA rows (bf16) arrive in that layout
-//             by TMA (one 2-D load per dim block of 64 rows, issued at
-//             set-up) and are converted in place; a row whose
-//             largest magnitude reaches 2^16 is first scaled by 2^-b (b <= 7,
-//             exact), and its logits and probabilities are scaled back by 2^b
-//             in the softmax (rows reaching 2^23 are reported as out of
-//             range). Below 2^-14 a value keeps an absolute accuracy of
-//             2^-25; absent rows are zero;
+//             then dequantised (E2M1 -> f16x2 hardware convert times the
+//             E4M3 scale as a packed f16 multiply: the product, <= 6
+//             significant bits in 2^-10 .. 2688, is exact in fp16) into one
+//             of two key buffers in the K-major 128-byte-swizzle layout
+//             [dim/64][key][128 B]. SWA rows (bf16) arrive in that layout by
+//             TMA (one 2-D load per dim block of 64 rows, issued at set-up)
+//             and are converted in place; a row whose largest magnitude
+//             reaches 2^16 is first scaled by 2^-b (b <= 7, exact), and its
+//             logits and probabilities are scaled back by 2^b in the softmax
+//             (rows reaching 2^23 are reported as out of range). Below 2^-14
+//             a value keeps an absolute accuracy of 2^-25; absent rows are
+//             zero;
 //   MMA (one thread each of warps 12 and 13): warp 12 issues
 //             S(t) = Q K(t)^T with tcgen05.mma kind::f16, M = 64 heads,
 //             N = 64 keys, K = 512, into one of two S buffers in TMEM, as
@@ -39,21 +38,24 @@
 //             tile exceeds it by more than 2^8 (probabilities stay <= 256)
 //             and writes P (fp16); in the rare case of a raised max, the same
 //             warps first rescale O in TMEM.
-// Each query head is converted to fp16 scaled by the power of two that puts
-// its largest magnitude in [2^14, 2^15), which is exact for every bf16 row;
-// the factor goes into that head's softmax scale.
+// Each query head is read from global memory and converted to fp16 (by the
+// softmax and MMA warps) scaled by the power of two that puts its largest
+// magnitude in [2^14, 2^15), which is exact for every bf16 row; the factor
+// goes into that head's softmax scale.
 // O for dims 0..255 accumulates in TMEM lanes 0..63 and dims 256..511 in
 // lanes 64..127 of the same 256 columns: two MMAs with A = [P; 0] and
 // A = [0; P] (zero rows leave the other half unchanged). P is stored once,
 // between two zero blocks, and each MMA's A starts at a different block.
 // TMEM: S at columns 0..63 and 64..127 (lanes 0-15 of each quadrant), O at
-// 256..511 (512 allocated, one CTA
-// per SM). Split-K partials (m, l, unnormalised O; O stored [dim/4][head][4]
-// so the epilogue's stores and the merge's loads are contiguous across heads)
-// are merged by the log-sum-exp merge kernel. Every wait is bounded; after a
-// timed-out wait the CTA reports CSA2_ERR_TIMEOUT and winds down (the warp
-// groups decide to stop by barrier reductions, so no warp is left behind at
-// a barrier).
+// 256..511 (512 allocated, one CTA per SM). Split-K partials (m, l,
+// unnormalised O; O stored [dim/4][head][4] so the epilogue's stores and the
+// merge's loads are contiguous across heads) are merged by the log-sum-exp
+// merge kernel. In a layer-group call the kernel starts early (see the
+// set-up): everything but the index reads and the global stores runs before
+// the wait for the Top-K kernels. Every wait is bounded; after a timed-out
+// wait the CTA reports CSA2_ERR_TIMEOUT and winds down (the warp groups
+// decide to stop by barrier reductions, so no warp is left behind at a
+// barrier).
 #include <cstring>
 
 #include "common.cuh"
