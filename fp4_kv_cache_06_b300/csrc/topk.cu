@@ -205,7 +205,9 @@ __global__ void __launch_bounds__(kTkThreads) k_topk_compact(const float* __rest
 }
 
 // ---- step 3 ----------------------------------------------------------------
-constexpr int kFinThreads = 1024;
+// The final kernel runs NT threads per row: 512 for k <= 512 (shorter
+// barriers; measured faster), 1024 for larger k (the pool's 2048).
+constexpr int kFinThreadsSmallK = 512, kFinThreadsLargeK = 1024;
 
 // Key sources for the radix select.
 struct SmemKeys {
@@ -229,7 +231,7 @@ struct RowKeys {
 
 // Exact key of the k-th largest among the source's keys (all distinct);
 // requires at least k keys. MSD radix, 8 bits per pass.
-template <class Src>
+template <int NT, class Src>
 __device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
   __shared__ uint64_t s_prefix;
   __shared__ int s_remaining;
@@ -241,7 +243,7 @@ __device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
   {
     unsigned long long a = ~0ull, o = 0ull;
     const int64_t m = src.size();
-    for (int64_t i = tid; i < m; i += kFinThreads) {
+    for (int64_t i = tid; i < m; i += NT) {
       uint64_t key;
       if (src.get(i, key)) { a &= key; o |= key; }
     }
@@ -260,11 +262,11 @@ __device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
   uint64_t prefix = s_and & mask;
   int remaining = k;
   for (int shift = start; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kFinThreads) h256[i] = 0;
+    for (int i = tid; i < 256; i += NT) h256[i] = 0;
     __syncthreads();
     const int64_t m = src.size();
     const int lane = tid & 31;
-    for (int64_t i0 = 0; i0 < m; i0 += kFinThreads) {
+    for (int64_t i0 = 0; i0 < m; i0 += NT) {
       const int64_t i = i0 + tid;
       uint64_t key = 0;
       const bool ok = i < m && src.get(i, key) && (key & mask) == prefix;
@@ -307,11 +309,12 @@ __device__ uint64_t radix_kth(const Src& src, int k, uint32_t* h256) {
 }
 
 // Bitonic sort of sel[0..np) ascending (np a power of two, padded with INT_MAX).
+template <int NT>
 __device__ void bitonic_sort_i32(int32_t* sel, int np) {
   for (int size = 2; size <= np; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       __syncthreads();
-      for (int i = threadIdx.x; i < np / 2; i += kFinThreads) {
+      for (int i = threadIdx.x; i < np / 2; i += NT) {
         const int lo = 2 * i - (i & (stride - 1));
         const int hi = lo + stride;
         const bool up = ((lo & size) == 0);
@@ -323,18 +326,18 @@ __device__ void bitonic_sort_i32(int32_t* sel, int np) {
   __syncthreads();
 }
 
-template <class Src>
+template <int NT, class Src>
 __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t* __restrict__ out,
                                  uint32_t* h256, int32_t* sel) {
   __shared__ uint32_t s_cnt;
   const int tid = threadIdx.x;
   uint64_t thr = 0;
-  if (n_keys > k) thr = radix_kth(src, k, h256);
+  if (n_keys > k) thr = radix_kth<NT>(src, k, h256);
   if (tid == 0) s_cnt = 0;
   __syncthreads();
   const int64_t m = src.size();
   const int lane = tid & 31;
-  for (int64_t i0 = 0; i0 < m; i0 += kFinThreads) {
+  for (int64_t i0 = 0; i0 < m; i0 += NT) {
     const int64_t i = i0 + tid;
     uint64_t key = 0;
     const bool take = i < m && src.get(i, key) && key >= thr;
@@ -354,19 +357,19 @@ __device__ void select_and_write(const Src& src, int k, int64_t n_keys, int32_t*
   if (k <= 512) {
     // ascending order by rank: the chosen positions are distinct, so the rank
     // of one is the number of chosen positions below it (reads broadcast)
-    for (int i = tid; i < cnt; i += kFinThreads) {
+    for (int i = tid; i < cnt; i += NT) {
       const int32_t mine = sel[i];
       int rank = 0;
       for (int j = 0; j < cnt; ++j) rank += sel[j] < mine;
       out[rank] = mine;
     }
-    for (int i = cnt + tid; i < k; i += kFinThreads) out[i] = -1;
+    for (int i = cnt + tid; i < k; i += NT) out[i] = -1;
   } else {
     int np = 1;
     while (np < k) np <<= 1;
-    for (int i = cnt + tid; i < np; i += kFinThreads) sel[i] = 0x7FFFFFFF;
-    bitonic_sort_i32(sel, np);
-    for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? sel[i] : -1;
+    for (int i = cnt + tid; i < np; i += NT) sel[i] = 0x7FFFFFFF;
+    bitonic_sort_i32<NT>(sel, np);
+    for (int i = tid; i < k; i += NT) out[i] = i < cnt ? sel[i] : -1;
   }
 }
 
@@ -418,23 +421,26 @@ __device__ void warp_digit_from_top(const uint32_t* h, uint32_t need, int* digit
 // Candidates keys[0..cnt) in index order with increasing positions, all at or
 // above threshold bin vbin: write the k best positions, ascending, to out.
 // h1, h2: two 1024-entry shared histograms; s_warp: the block scan's scratch.
+template <int NT>
 __device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, int32_t* __restrict__ out,
                                uint32_t* h1, uint32_t* h2, uint32_t* s_warp) {
   __shared__ uint32_t s_above, s_aA, s_aB;
   __shared__ int s_dA, s_dB;
   const int tid = threadIdx.x, lane = tid & 31;
   if (cnt <= k) {
-    for (int i = tid; i < k; i += kFinThreads) out[i] = i < cnt ? cand_pos_of(keys[i]) : -1;
+    for (int i = tid; i < k; i += NT) out[i] = i < cnt ? cand_pos_of(keys[i]) : -1;
     return;
   }
-  h1[tid] = 0;
-  h2[tid] = 0;
+  for (int i = tid; i < 1024; i += NT) {
+    h1[i] = 0;
+    h2[i] = 0;
+  }
   if (tid == 0) s_above = 0;
   __syncthreads();
   // entries above the threshold bin are all taken; score-key bits 19..10 of
   // the entries in it
   uint32_t above = 0;
-  for (int i = tid; i < cnt; i += kFinThreads) {
+  for (int i = tid; i < cnt; i += NT) {
     const uint64_t key = keys[i];
     const int bin = (int)(key >> 52);
     if (bin > vbin) ++above;
@@ -454,7 +460,7 @@ __device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, i
   const uint32_t need = (uint32_t)k - s_above - s_aA;
   const uint64_t preA = ((uint64_t)vbin << 10) | (uint64_t)s_dA;   // score key >> 10
   // score-key bits 9..0 of the entries sharing that prefix
-  for (int i = tid; i < cnt; i += kFinThreads) {
+  for (int i = tid; i < cnt; i += NT) {
     const uint64_t key = keys[i];
     if ((key >> 42) == preA) atomicAdd(&h2[(key >> 32) & 1023], 1u);
   }
@@ -472,7 +478,7 @@ __device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, i
   // counts (strictly above | ties << 16; both < 2^16) gives both prefixes:
   // the entry's slot is (above before it) + min(ties before it, r), as ties
   // at thr go to the first r in index order.
-  const int S = (cnt + kFinThreads - 1) / kFinThreads;
+  const int S = (cnt + NT - 1) / NT;
   const int lo = min(tid * S, cnt), hi = min(lo + S, cnt);
   uint32_t gt = 0, ties = 0;
   for (int i = lo; i < hi; ++i) {
@@ -481,7 +487,7 @@ __device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, i
     ties += sk == thr;
   }
   uint32_t tot;
-  const uint32_t pre = block_excl_scan<kFinThreads>(gt | (ties << 16), s_warp, &tot);
+  const uint32_t pre = block_excl_scan<NT>(gt | (ties << 16), s_warp, &tot);
   uint32_t tr = pre >> 16;
   uint32_t o = (pre & 0xFFFFu) + min(tr, r);
   for (int i = lo; i < hi; ++i) {
@@ -495,7 +501,8 @@ __device__ void ordered_select(const uint64_t* keys, int cnt, int vbin, int k, i
 // Gather modes of step 3.
 enum FinalMode : int { kFinDirect = 0, kFinTable = 1, kFinUnordered = 2 };
 
-__global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restrict__ scores,
+template <int NT>
+__global__ void __launch_bounds__(NT) k_topk_final(const float* __restrict__ scores,
                                                             const int32_t* __restrict__ cand_pos,
                                                             int64_t stride, const int64_t* __restrict__ n,
                                                             int len_div, int64_t n_max, int k,
@@ -509,7 +516,7 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
   int32_t* sel = reinterpret_cast<int32_t*>(h + 1024);                // kMaxTopK
   uint32_t* pre = reinterpret_cast<uint32_t*>(sel + kMaxTopK);        // kMaxChunks
   uint32_t* cbase = pre + kMaxChunks;                                 // kMaxChunks
-  __shared__ uint32_t s_warp[kFinThreads / 32];
+  __shared__ uint32_t s_warp[NT / 32];
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -530,11 +537,11 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
     if (tid == 0) s_valid = 0;
     __syncthreads();
     uint32_t loc = 0;
-    for (int64_t i = tid; i < nb; i += kFinThreads) loc += (cp == nullptr || cp[i] >= 0);
+    for (int64_t i = tid; i < nb; i += NT) loc += (cp == nullptr || cp[i] >= 0);
     atomicAdd(&s_valid, loc);
     __syncthreads();
     RowKeys src{s, cp, nb};
-    select_and_write(src, k, (int64_t)s_valid, out, h, sel);
+    select_and_write<NT>(src, k, (int64_t)s_valid, out, h, sel);
     return;
   }
   const int vbin = (int)hv.w;
@@ -543,17 +550,17 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
     // the row itself, in index order: entries at or above the threshold bin;
     // the next 8192 entries load while these are compacted
     uint32_t run = 0;
-    for (int64_t i0 = 0; i0 < nb; i0 += (int64_t)kFinThreads * 8) {
+    for (int64_t i0 = 0; i0 < nb; i0 += (int64_t)NT * 8) {
       float vn[8];
       int32_t pn[8];
-      const int64_t nxt = i0 + (int64_t)kFinThreads * 8;
+      const int64_t nxt = i0 + (int64_t)NT * 8;
       if (nxt < nb) load8(s, cp, nxt + (int64_t)tid * 8, nb, vn, pn);
       uint32_t take = 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         if (p[u] >= 0 && (int)(score_key(v[u]) >> 20) >= vbin) take |= 1u << u;
       uint32_t tot;
-      uint32_t slot = run + block_excl_scan<kFinThreads>(__popc(take), s_warp, &tot);
+      uint32_t slot = run + block_excl_scan<NT>(__popc(take), s_warp, &tot);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         if (!((take >> u) & 1)) continue;
@@ -571,7 +578,7 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
     // chunk order is index order: prefix of the chunk counts, then one
     // binary search per candidate into the prefix
     const int nch = (int)((nb + kChunk - 1) / kChunk);
-    constexpr int kPer = kMaxChunks / kFinThreads;
+    constexpr int kPer = kMaxChunks / NT;
     uint2 e[kPer];
     uint32_t sum = 0;
 #pragma unroll
@@ -581,7 +588,7 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
       sum += e[u].y;
     }
     uint32_t tot;
-    uint32_t run = block_excl_scan<kFinThreads>(sum, s_warp, &tot);
+    uint32_t run = block_excl_scan<NT>(sum, s_warp, &tot);
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int c = tid * kPer + u;
@@ -591,11 +598,11 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
     __syncthreads();
     cnt = (int)min(tot, (uint32_t)kCandCap);
     const uint64_t* rc = cand + (int64_t)b * kCandCap;
-    constexpr int kG = kCandCap / kFinThreads;
+    constexpr int kG = kCandCap / NT;
     uint64_t kv[kG];
 #pragma unroll
     for (int u = 0; u < kG; ++u) {
-      const int o = tid + u * kFinThreads;
+      const int o = tid + u * NT;
       kv[u] = 0;
       if (o < cnt) {
         int lo = 0, hi = nch - 1;                     // last chunk with pre <= o
@@ -609,27 +616,27 @@ __global__ void __launch_bounds__(kFinThreads) k_topk_final(const float* __restr
     }
 #pragma unroll
     for (int u = 0; u < kG; ++u) {
-      const int o = tid + u * kFinThreads;
+      const int o = tid + u * NT;
       if (o < cnt) keys[o] = kv[u];
     }
   } else {
     cnt = (int)min(hv.x, (uint32_t)kCandCap);
-    for (int i = tid; i < cnt; i += kFinThreads) keys[i] = cand[(int64_t)b * kCandCap + i];
+    for (int i = tid; i < cnt; i += NT) keys[i] = cand[(int64_t)b * kCandCap + i];
   }
   __syncthreads();
   // positions increasing along the candidates: select in order, no sort
   bool mono = mode != kFinUnordered;
   if (mono) {
-    const int S = (cnt + kFinThreads - 1) / kFinThreads;
+    const int S = (cnt + NT - 1) / NT;
     const int lo = min(tid * S, cnt), hi = min(lo + S + 1, cnt);
     for (int i = lo + 1; i < hi; ++i)
       if (cand_pos_of(keys[i - 1]) >= cand_pos_of(keys[i])) mono = false;
   }
   if (__syncthreads_and(mono)) {
-    ordered_select(keys, cnt, vbin, k, out, h, pre, s_warp);   // the chunk prefix is no longer needed
+    ordered_select<NT>(keys, cnt, vbin, k, out, h, pre, s_warp);   // the chunk prefix is no longer needed
   } else {
     SmemKeys src{keys, cnt};
-    select_and_write(src, k, cnt, out, h, sel);
+    select_and_write<NT>(src, k, cnt, out, h, sel);
   }
 }
 
@@ -700,7 +707,10 @@ int launch_topk(const float* scores, const int32_t* cand_pos, int64_t stride, co
     count_launch();
     if ((rc = launch_status(e)) != CSA2_OK) return rc;
   }
-  const cudaError_t e = launch_pdl(k_topk_final, dim3((unsigned)B), dim3(kFinThreads), (size_t)topk_final_smem(), s,
+  const bool small_k = k <= 512;
+  const cudaError_t e = launch_pdl(small_k ? k_topk_final<kFinThreadsSmallK> : k_topk_final<kFinThreadsLargeK>,
+                                   dim3((unsigned)B), dim3(small_k ? kFinThreadsSmallK : kFinThreadsLargeK),
+                                   (size_t)topk_final_smem(), s,
                                    scores, cand_pos, stride, n, len_div, n_max, k,
                                    static_cast<const TopkHdr*>(w.hdr), static_cast<const uint64_t*>(w.cand),
                                    static_cast<const uint2*>(w.tab), mode, idx_out);
@@ -734,9 +744,9 @@ int launch_pool_block_max(const float* scores, int64_t stride, const int64_t* n,
 }
 
 int topk_init_attributes() {
-  if (cudaFuncSetAttribute(k_topk_final, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           topk_final_smem()) != cudaSuccess)
-    return CSA2_ERR_CUDA;
+  for (auto kern : {k_topk_final<kFinThreadsSmallK>, k_topk_final<kFinThreadsLargeK>})
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, topk_final_smem()) != cudaSuccess)
+      return CSA2_ERR_CUDA;
   return CSA2_OK;
 }
 
