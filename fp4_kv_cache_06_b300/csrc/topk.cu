@@ -20,7 +20,8 @@
 //      chunks of kChunk entries; a CTA compacts a chunk (the entries at or
 //      above the threshold bin, in index order), reserves room for it with a
 //      single atomic and records (base, count) in the row's chunk table;
-//   3. one CTA per row gathers the candidates in index order (through the
+//   3. one CTA per row (512 threads for k <= 512, 1024 above) gathers the
+//      candidates in index order (through the
 //      chunk table, or straight from the row when it is short). When the
 //      positions increase with the index (position-indexed rows, pool slots)
 //      the k-th score is resolved inside the threshold bin by two 10-bit
